@@ -1,0 +1,25 @@
+"""GB300-native block-scaled FP8 MoE expert library (sm_103a).
+
+The compute path lives in ``libmoe_fp8.so`` (CUDA kernels behind the C ABI of
+``include/moe_fp8.h``); ``_lib`` is its ctypes binding, ``problem`` assembles
+device buffers for a workload using only the library's kernels, and
+``workloads`` draws the seeded synthetic inputs.
+"""
+
+from ._lib import (  # noqa: F401
+    MoeError,
+    MoeFwdArgs,
+    load,
+    make_fwd_args,
+    moe_forward_workspace_size,
+    moe_fp8_block_scale_forward,
+    moe_plan,
+    moe_plan_capacity,
+    moe_plan_workspace_size,
+    moe_prep_weights,
+    moe_quantize_act_1x128,
+    moe_quantize_weight_128x128,
+    moe_requant_scales_ue8m0,
+    moe_status_string,
+    moe_workspace_init,
+)

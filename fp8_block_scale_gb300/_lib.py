@@ -1,0 +1,204 @@
+"""ctypes binding of libmoe_fp8.so (the C ABI declared in include/moe_fp8.h).
+
+Argument marshalling only: every function forwards device pointers, sizes
+and the current torch stream to the C entry point of the same name and raises
+``MoeError`` on a non-zero status.  There is no fallback: if the shared
+library is missing, loading fails loudly.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_fp8.so")
+
+MOE_OK = 0
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_ALIGN", 4: "MOE_ERR_CAPACITY",
+    5: "MOE_ERR_DTYPE", 6: "MOE_ERR_DEVICE", 7: "MOE_ERR_CUDA", 8: "MOE_ERR_TIMEOUT",
+}
+MOE_DEV_TIMEOUT = 0x1
+MOE_DEV_BAD_EXPERT = 0x2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+class MoeFwdArgs(ctypes.Structure):
+    """Mirror of ``struct moe_fwd_args``."""
+    _fields_ = [
+        ("a", ctypes.c_void_p),
+        ("a_scale", ctypes.c_void_p),
+        ("w13", ctypes.c_void_p),
+        ("w13_scale", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p),
+        ("topk_weights", ctypes.c_void_p),
+        ("sorted_token_ids", ctypes.c_void_p),
+        ("expert_ids", ctypes.c_void_p),
+        ("num_tokens_post_padded", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("device_status", ctypes.c_void_p),
+        ("debug_q_inter", ctypes.c_void_p),
+        ("debug_s_inter", ctypes.c_void_p),
+        ("M", ctypes.c_int64),
+        ("sorted_cap", ctypes.c_int64),
+        ("blocks_cap", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("H", ctypes.c_int32),
+        ("I", ctypes.c_int32),
+        ("E", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
+        ("block_m", ctypes.c_int32),
+        ("routed_scale", ctypes.c_float),
+    ]
+
+
+_lib = None
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_plan_capacity": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+    "moe_plan_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int]),
+    "moe_plan": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_prep_weights": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p]),
+    "moe_requant_scales_ue8m0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "moe_quantize_act_1x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_quantize_weight_128x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_forward_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int64]),
+    "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_fp8_block_scale_forward": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
+}
+
+
+def load(path=LIB_PATH):
+    """Load libmoe_fp8.so (built by ``fp8_block_scale_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def moe_status_string(status):
+    return load().moe_status_string(status).decode()
+
+
+def moe_plan_capacity(M, top_k, E, block_m):
+    cap = ctypes.c_int64()
+    blocks = ctypes.c_int64()
+    _check("moe_plan_capacity", load().moe_plan_capacity(M, top_k, E, block_m, ctypes.byref(cap), ctypes.byref(blocks)))
+    return cap.value, blocks.value
+
+
+def moe_plan_workspace_size(M, top_k, E):
+    return load().moe_plan_workspace_size(M, top_k, E)
+
+
+def moe_plan(topk_ids, E, block_m, sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, stream=None):
+    M, top_k = topk_ids.shape
+    bits = {torch.int32: 32, torch.int64: 64}[topk_ids.dtype]
+    _check("moe_plan", load().moe_plan(
+        _ptr(topk_ids), bits, M, top_k, E, block_m, _ptr(sorted_token_ids), sorted_token_ids.numel(),
+        _ptr(expert_ids), expert_ids.numel(), _ptr(num_tokens_post_padded), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_prep_weights(w13, w13_interleaved, stream=None):
+    E, N, H = w13.shape
+    _check("moe_prep_weights", load().moe_prep_weights(_ptr(w13), _ptr(w13_interleaved), E, N, H, _stream(stream)))
+
+
+def moe_requant_scales_ue8m0(w, scale, ue8m0_exp=None, stream=None):
+    E, rows, cols = w.shape
+    _check("moe_requant_scales_ue8m0", load().moe_requant_scales_ue8m0(
+        _ptr(w), _ptr(scale), _ptr(ue8m0_exp), E, rows, cols, _stream(stream)))
+
+
+def moe_quantize_act_1x128(x_bf16, q, scale, stream=None):
+    M, H = x_bf16.shape
+    _check("moe_quantize_act_1x128", load().moe_quantize_act_1x128(
+        _ptr(x_bf16), M, H, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_weight_128x128(w_bf16, q, scale, stream=None):
+    E, rows, cols = w_bf16.shape
+    _check("moe_quantize_weight_128x128", load().moe_quantize_weight_128x128(
+        _ptr(w_bf16), E, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_forward_workspace_size(M, H, I, top_k, block_m, sorted_cap):
+    return load().moe_forward_workspace_size(M, H, I, top_k, block_m, sorted_cap)
+
+
+def moe_workspace_init(workspace, stream=None):
+    _check("moe_workspace_init", load().moe_workspace_init(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def make_fwd_args(a, a_scale, w13, w13_scale, w2, w2_scale, topk_weights, sorted_token_ids, expert_ids,
+                  num_tokens_post_padded, out, workspace, top_k, block_m, routed_scale=1.0,
+                  device_status=None, debug_q_inter=None, debug_s_inter=None):
+    """Fill a ``moe_fwd_args`` from tensors (shapes give the sizes)."""
+    M, H = a.shape
+    E, N, _ = w13.shape
+    args = MoeFwdArgs()
+    args.a, args.a_scale = a.data_ptr(), a_scale.data_ptr()
+    args.w13, args.w13_scale = w13.data_ptr(), w13_scale.data_ptr()
+    args.w2, args.w2_scale = w2.data_ptr(), w2_scale.data_ptr()
+    args.topk_weights = topk_weights.data_ptr()
+    args.sorted_token_ids = sorted_token_ids.data_ptr()
+    args.expert_ids = expert_ids.data_ptr()
+    args.num_tokens_post_padded = num_tokens_post_padded.data_ptr()
+    args.out = out.data_ptr()
+    args.workspace = workspace.data_ptr()
+    args.device_status = device_status.data_ptr() if device_status is not None else None
+    args.debug_q_inter = debug_q_inter.data_ptr() if debug_q_inter is not None else None
+    args.debug_s_inter = debug_s_inter.data_ptr() if debug_s_inter is not None else None
+    args.M = M
+    args.sorted_cap = sorted_token_ids.numel()
+    args.blocks_cap = expert_ids.numel()
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    args.H, args.I, args.E = H, N // 2, E
+    args.top_k, args.block_m = top_k, block_m
+    args.routed_scale = routed_scale
+    return args
+
+
+def moe_fp8_block_scale_forward(args, stream=None):
+    _check("moe_fp8_block_scale_forward", load().moe_fp8_block_scale_forward(ctypes.byref(args), _stream(stream)))

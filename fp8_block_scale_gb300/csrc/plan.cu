@@ -1,0 +1,213 @@
+// moe_plan: the moe_align_block_size routing plan on the device (FlashInfer
+// PR #4287 commit summary: routes sorted per expert and padded to block_m;
+// "Public contract and review fixes": sorted_token_ids holds
+// expert_ids.numel() * block_m slots).
+//
+// Deterministic three-launch counting sort:
+//   1. rank:    each CTA takes a chunk of kChunk routes, computes every route's
+//               stable rank among same-expert routes of its chunk (warp
+//               match + per-warp histograms in shared memory) and the chunk's
+//               per-expert counts.
+//   2. scan:    one CTA turns the [chunks x E] counts into per-chunk bases,
+//               pads each expert to block_m, scans the experts, writes
+//               expert_ids, the pad sentinels and P.
+//   3. scatter: sorted_token_ids[base(chunk, e) + rank] = r.
+// No inter-CTA waits; the same ids always give the same bytes.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 512;  // routes per CTA in the rank/scatter launches (one per thread)
+constexpr int kChunkWarps = kChunk / 32;
+constexpr int kScanThreads = 1024;
+constexpr int kMaxExperts = 2048;
+
+struct PlanWs {
+  int32_t* counts;  // [chunks, E]: chunk counts, then absolute bases
+  int32_t* rank;    // [R] stable rank of each route inside its chunk (or -1)
+  int32_t* seg;     // [E] segment start of each expert
+};
+
+__device__ __forceinline__ int load_id(const void* ids, int id_bits, int64_t r, int E) {
+  int64_t v = id_bits == 64 ? static_cast<const int64_t*>(ids)[r] : static_cast<const int32_t*>(ids)[r];
+  return (v >= 0 && v < E) ? static_cast<int>(v) : -1;
+}
+
+__global__ void __launch_bounds__(kChunk) plan_rank_kernel(const void* ids, int id_bits, int64_t R, int E, PlanWs ws) {
+  extern __shared__ int32_t wh[];  // [kChunkWarps][E]
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kChunk + threadIdx.x;
+  const int e = r < R ? load_id(ids, id_bits, r, E) : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned below = peers & ((1u << lane) - 1u);
+  const int in_warp = __popc(below);
+  if (e >= 0 && below == 0) wh[warp * E + e] = __popc(peers);
+  __syncthreads();
+  // exclusive scan over warps, per expert; chunk total goes to counts
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kChunkWarps; ++w) {
+      const int v = wh[w * E + x];
+      wh[w * E + x] = run;
+      run += v;
+    }
+    ws.counts[static_cast<int64_t>(blockIdx.x) * E + x] = run;
+  }
+  __syncthreads();
+  if (r < R) ws.rank[r] = e >= 0 ? wh[warp * E + e] + in_warp : -1;
+}
+
+// Block-wide exclusive scan of one int per thread (kScanThreads threads).
+__device__ int block_exclusive_scan(int v, int* total, int* smem /* 32 ints */) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) smem[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = smem[lane];
+    int winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += n;
+    }
+    smem[lane] = winc - w;  // exclusive prefix of warp sums
+    if (lane == 31) smem[32] = winc;
+  }
+  __syncthreads();
+  const int res = smem[warp] + inc - v;
+  *total = smem[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int E, int block_m, int nchunks, PlanWs ws,
+                                                                  int32_t* sorted_ids, int32_t* expert_ids,
+                                                                  int32_t* num_post_padded) {
+  __shared__ int scan_smem[33];
+  constexpr int kPer = kMaxExperts / kScanThreads;  // experts per thread (2)
+  int total[kPer], padded[kPer];
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x * kPer + i;
+    int run = 0;
+    if (e < E) {
+      for (int c = 0; c < nchunks; ++c) {
+        int32_t* p = ws.counts + static_cast<int64_t>(c) * E + e;
+        const int v = *p;
+        *p = run;  // exclusive base inside the expert
+        run += v;
+      }
+    }
+    total[i] = run;
+    padded[i] = (run + block_m - 1) / block_m * block_m;
+    mine += padded[i];
+  }
+  int P = 0;
+  int start = block_exclusive_scan(mine, &P, scan_smem);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x * kPer + i;
+    if (e < E) {
+      ws.seg[e] = start;
+      for (int s = start + total[i]; s < start + padded[i]; ++s) sorted_ids[s] = static_cast<int32_t>(R);
+      for (int b = start / block_m; b < (start + padded[i]) / block_m; ++b) expert_ids[b] = e;
+    }
+    start += padded[i];
+  }
+  if (threadIdx.x == 0) *num_post_padded = P;
+}
+
+__global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, int id_bits, int64_t R, int E, PlanWs ws,
+                                                               int32_t* sorted_ids) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kChunk + threadIdx.x;
+  if (r >= R) return;
+  const int rk = ws.rank[r];
+  if (rk < 0) return;
+  const int e = load_id(ids, id_bits, r, E);
+  const int base = ws.seg[e] + ws.counts[static_cast<int64_t>(blockIdx.x) * E + e];
+  sorted_ids[base + rk] = static_cast<int32_t>(r);
+}
+
+size_t plan_ws_bytes(int64_t R, int E, int64_t* nchunks_out) {
+  const int64_t nchunks = ceil_div(R > 0 ? R : 1, kChunk);
+  if (nchunks_out) *nchunks_out = nchunks;
+  return static_cast<size_t>(round_up(nchunks * E * 4, 256) + round_up(R * 4, 256) + round_up(E * 4, 256));
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_plan_workspace_size(int64_t M, int top_k, int E) {
+  if (M < 0 || top_k < 1 || E < 1) return 0;
+  return moe::plan_ws_bytes(M * top_k, E, nullptr);
+}
+
+moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int E, int block_m,
+                    int32_t* sorted_token_ids, int64_t sorted_cap, int32_t* expert_ids, int64_t blocks_cap,
+                    int32_t* num_tokens_post_padded, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  using namespace moe;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded || !workspace) return MOE_ERR_NULL;
+  if (id_bits != 32 && id_bits != 64) return MOE_ERR_DTYPE;
+  if (M < 0 || top_k < 1 || E < 1 || E > kMaxExperts) return MOE_ERR_SHAPE;
+  if (block_m < 8 || block_m > 1024 || block_m % 8 != 0) return MOE_ERR_SHAPE;
+  const int64_t R = M * top_k;
+  if (R >= (int64_t(1) << 31) - 1) return MOE_ERR_SHAPE;
+  if (R > 0 && !topk_ids) return MOE_ERR_NULL;
+  int64_t need_cap = 0, need_blocks = 0;
+  moe_plan_capacity(M, top_k, E, block_m, &need_cap, &need_blocks);
+  if (sorted_cap < need_cap || blocks_cap < need_blocks) return MOE_ERR_CAPACITY;
+  int64_t nchunks = 0;
+  if (workspace_bytes < plan_ws_bytes(R, E, &nchunks)) return MOE_ERR_CAPACITY;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if ((R > 0 && !on_device(topk_ids, dev.device)) || !on_device(sorted_token_ids, dev.device) ||
+      !on_device(expert_ids, dev.device) || !on_device(num_tokens_post_padded, dev.device) ||
+      !on_device(workspace, dev.device))
+    return MOE_ERR_DEVICE;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  PlanWs ws;
+  ws.counts = reinterpret_cast<int32_t*>(w);
+  w += round_up(nchunks * E * 4, 256);
+  ws.rank = reinterpret_cast<int32_t*>(w);
+  w += round_up(R * 4, 256);
+  ws.seg = reinterpret_cast<int32_t*>(w);
+
+  const size_t smem = static_cast<size_t>(kChunkWarps) * E * sizeof(int32_t);
+  static bool attr_set[64] = {};
+  if (!attr_set[dev.device]) {
+    MOE_CUDA_TRY(cudaFuncSetAttribute(plan_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kChunkWarps * kMaxExperts * 4));
+    attr_set[dev.device] = true;
+  }
+  if (R > 0) {
+    plan_rank_kernel<<<static_cast<unsigned>(nchunks), kChunk, smem, stream>>>(topk_ids, id_bits, R, E, ws);
+    MOE_CUDA_TRY(cudaGetLastError());
+  } else {
+    nchunks = 0;
+  }
+  plan_scan_kernel<<<1, kScanThreads, 0, stream>>>(R, E, block_m, static_cast<int>(nchunks), ws, sorted_token_ids,
+                                                   expert_ids, num_tokens_post_padded);
+  MOE_CUDA_TRY(cudaGetLastError());
+  if (R > 0) {
+    plan_scatter_kernel<<<static_cast<unsigned>(nchunks), kChunk, 0, stream>>>(topk_ids, id_bits, R, E, ws,
+                                                                               sorted_token_ids);
+    MOE_CUDA_TRY(cudaGetLastError());
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+/*
+ * moe_fp8.h -- C ABI of the block-scaled FP8 MoE expert library for GB300
+ * (sm_103a).
+ *
+ * The library computes the routed MoE expert layer with FP8 (E4M3) operands
+ * and FP32 block scales, as described by FlashInfer pull request #4287
+ * ("feat(cake_alpha_moe): add optimized Blackwell W8A8 expert up/down
+ * compute": commit summary; PR description, "Public contract and review
+ * fixes") and SGLang pull request #43556 ("Requantize block-FP8 MoE weights
+ * to UE8M0 for DeepGEMM": "Motivation", "Modifications").
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers on the current CUDA device unless the
+ *    argument says otherwise; the caller owns every buffer.  The library
+ *    allocates no device memory and keeps no per-call global state.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are detected on the host and returned
+ *    before anything is launched; a failed launch returns MOE_ERR_CUDA.
+ *  - Conditions that only the device can see (a bounded wait that ran out, an
+ *    out-of-range expert id in a plan) are OR-ed into *device_status where an
+ *    entry point takes one (see MOE_DEV_* bits); nothing traps.
+ *  - Layouts are dense row-major.  E4M3 codes are uint8 bytes; BF16 values are
+ *    passed as their uint16 bit patterns.
+ */
+#ifndef MOE_FP8_H
+#define MOE_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,     /* a required pointer is NULL                         */
+  MOE_ERR_SHAPE = 2,    /* a size violates the documented constraints         */
+  MOE_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned                   */
+  MOE_ERR_CAPACITY = 4, /* plan or workspace buffers too small                */
+  MOE_ERR_DTYPE = 5,    /* unsupported id width                               */
+  MOE_ERR_DEVICE = 6,   /* pointer not on the current device / not sm_100+    */
+  MOE_ERR_CUDA = 7,     /* a CUDA runtime/driver call failed                  */
+  MOE_ERR_TIMEOUT = 8   /* reserved for host-visible timeouts                 */
+} moe_status;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define MOE_DEV_TIMEOUT 0x1         /* a bounded pipeline wait ran out; the CTA stopped */
+#define MOE_DEV_BAD_EXPERT 0x2      /* a plan block named an expert outside [0, E) other than -1 */
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * Routing plan (the moe_align_block_size plan; PR #4287 commit summary and
+ * "Public contract and review fixes").
+ *
+ * Route r = t * top_k + j sends token t to expert topk_ids[t, j].  The plan
+ * lists, expert by expert in ascending order, the route indices r of each
+ * expert in ascending order, padded with the sentinel R = M * top_k up to a
+ * multiple of block_m.  expert_ids[b] is the expert of block b and
+ * *num_tokens_post_padded = P, the padded length.  Ids outside [0, E)
+ * (including -1, "masked") are dropped.  Slots at and past P (and blocks at
+ * and past P / block_m) are NOT written: the caller may leave garbage there.
+ * ------------------------------------------------------------------------ */
+
+/* Worst-case (tight) sizes of the plan buffers: sorted_cap =
+ * roundup(R + min(E, R) * (block_m - 1), block_m), blocks_cap = sorted_cap /
+ * block_m.  Host-only; writes through the two host pointers. */
+moe_status moe_plan_capacity(int64_t M, int top_k, int E, int block_m,
+                             int64_t* sorted_cap, int64_t* blocks_cap);
+
+/* Device workspace bytes moe_plan needs for these sizes (host-only). */
+size_t moe_plan_workspace_size(int64_t M, int top_k, int E);
+
+/* Build the plan on the device.
+ *  topk_ids              [M, top_k] int32 (id_bits 32) or int64 (id_bits 64)
+ *  sorted_token_ids      [sorted_cap] int32 out
+ *  expert_ids            [blocks_cap] int32 out
+ *  num_tokens_post_padded [1] int32 out (device scalar)
+ *  workspace             >= moe_plan_workspace_size bytes, any contents
+ * Constraints: 1 <= E <= 2048; 8 <= block_m <= 1024, block_m % 8 == 0;
+ * sorted_cap and blocks_cap at least the moe_plan_capacity values.
+ * Deterministic: the same ids give the same bytes. */
+moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int E,
+                    int block_m, int32_t* sorted_token_ids, int64_t sorted_cap,
+                    int32_t* expert_ids, int64_t blocks_cap,
+                    int32_t* num_tokens_post_padded, void* workspace,
+                    size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Offline weight preparation.
+ * ------------------------------------------------------------------------ */
+
+/* Gate/up eight-row interleave ("Gate/up rows use the provided eight-row
+ * interleave", PR #4287 "Public contract and review fixes").  w13 holds
+ * [E, 2I, H] E4M3 codes in the logical layout (gate rows [0, I), up rows
+ * [I, 2I)); w13_interleaved receives, per expert, rows 16q..16q+7 = gate rows
+ * 8q..8q+7 and rows 16q+8..16q+15 = up rows I+8q..I+8q+7.  Out of place (the
+ * two buffers must not overlap).  Scales are NOT interleaved: the forward
+ * keeps reading w13_scale in the logical [E, 2I/128, H/128] layout.
+ * Constraints: N = 2I, I % 128 == 0, H % 16 == 0, 16-byte aligned pointers. */
+moe_status moe_prep_weights(const uint8_t* w13, uint8_t* w13_interleaved,
+                            int E, int N, int H, moe_stream_t stream);
+
+/* Power-of-two (UE8M0) block-scale requant, in place (SGLang PR #43556,
+ * "Motivation": grouped FP8 GEMMs that take UE8M0 scales need scales that are
+ * powers of two).  For every 128x128 block with FP32 scale s > 0:
+ * s' = 2^ceil(log2 s) (rounded up) and every code w becomes
+ * E4M3_rn_satfinite(f32(decode(w) * f32(s / s'))).  Blocks with s <= 0 or a
+ * non-finite s are left unchanged.
+ *  w          [E, rows, cols] E4M3 codes, rewritten in place
+ *  scale      [E, rows/128, cols/128] FP32, rewritten in place
+ *  ue8m0_exp  nullable [E, rows/128, cols/128] uint8 out: log2(s') + 127
+ *             clamped to [0, 254]; 0 for blocks left unchanged.
+ * Constraints: rows % 128 == 0, cols % 128 == 0. */
+moe_status moe_requant_scales_ue8m0(uint8_t* w, float* scale, uint8_t* ue8m0_exp,
+                                    int E, int rows, int cols, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Quantisers (the step before the path: "FP8 activations [M, K] with FP32
+ * per-token group-128 scales; FP8 weights with FP32 128x128 block scales",
+ * PR #4287 "Public contract and review fixes").  scale = f32(amax / 448);
+ * code = E4M3_rn_satfinite(f32(x / scale)) with an IEEE FP32 division; a
+ * group whose amax is 0 gets scale 0 and all-zero codes.
+ * ------------------------------------------------------------------------ */
+
+/* x [M, H] BF16 bits -> q [M, H] E4M3, scale [M, H/128] FP32.  H % 128 == 0. */
+moe_status moe_quantize_act_1x128(const uint16_t* x, int64_t M, int H,
+                                  uint8_t* q, float* scale, moe_stream_t stream);
+
+/* w [E, rows, cols] BF16 bits -> q [E, rows, cols] E4M3,
+ * scale [E, rows/128, cols/128] FP32.  rows, cols % 128 == 0. */
+moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, int cols,
+                                       uint8_t* q, float* scale, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The fused forward (PR #4287 commit summary and "Public contract and review
+ * fixes"; post-dot scale application, "Final W8 kernel performance (v46)").
+ *
+ * For every plan block b < P / block_m whose expert e = expert_ids[b] is in
+ * [0, E), and every slot whose route id r = sorted_token_ids[slot] < R, with
+ * token t = r / top_k:
+ *   g|u[n] = sum_kb f32(dot128(a[t], w13[e, n])) * a_scale[t, kb] * w13_scale[e, n/128, kb]
+ *   h[i]   = silu(gate[i]) * up[i]
+ *   q, s   = per-128-column E4M3 requant of h (scale amax/448; zero -> 0)
+ *   y[c]   = sum_ib f32(dot128(q, w2[e, c])) * s[ib] * w2_scale[e, c/128, ib]
+ *   out[t, c] += y[c] * topk_weights[t, j] * routed_scale
+ * The route contributions are summed in FP32 and `out` is rounded to BF16
+ * once per call: out = bf16_rn(f32(out) + sum).  Blocks past P exit
+ * untouched; pad slots (id >= R) contribute nothing.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_fwd_args {
+  const uint8_t* a;                        /* [M, H] E4M3 activations                       */
+  const float* a_scale;                    /* [M, H/128] FP32 per-token group scales        */
+  const uint8_t* w13;                      /* [E, 2I, H] E4M3, interleaved by moe_prep_weights */
+  const float* w13_scale;                  /* [E, 2I/128, H/128] FP32, LOGICAL row blocks   */
+  const uint8_t* w2;                       /* [E, H, I] E4M3                                */
+  const float* w2_scale;                   /* [E, H/128, I/128] FP32                        */
+  const float* topk_weights;               /* [M, top_k] FP32 route weights                 */
+  const int32_t* sorted_token_ids;         /* [sorted_cap] plan (moe_plan)                  */
+  const int32_t* expert_ids;               /* [blocks_cap] plan                             */
+  const int32_t* num_tokens_post_padded;   /* [1] device scalar P; never read on the host   */
+  uint16_t* out;                           /* [M, H] BF16 bits, accumulated in place        */
+  void* workspace;                         /* moe_forward_workspace_size bytes, zeroed once */
+  int32_t* device_status;                  /* nullable [1]: MOE_DEV_* bits are OR-ed in     */
+  uint8_t* debug_q_inter;                  /* nullable [sorted_cap, I]: intermediate codes  */
+  float* debug_s_inter;                    /* nullable [sorted_cap, I/128]: their scales    */
+  int64_t M;                               /* tokens                                        */
+  int64_t sorted_cap;                      /* length of sorted_token_ids                    */
+  int64_t blocks_cap;                      /* length of expert_ids                          */
+  size_t workspace_bytes;
+  int32_t H;                               /* hidden size (K of the gate/up GEMM)           */
+  int32_t I;                               /* intermediate size (gate/up width N = 2I)      */
+  int32_t E;                               /* experts                                       */
+  int32_t top_k;
+  int32_t block_m;
+  float routed_scale;                      /* routed scaling factor (1.0 = none)            */
+} moe_fwd_args;
+
+/* Workspace bytes the forward needs (host-only).  The workspace holds the
+ * requantised intermediate (sorted_cap x I codes and sorted_cap x I/128
+ * scales) and an FP32 [M, H] route accumulator. */
+size_t moe_forward_workspace_size(int64_t M, int H, int I, int top_k, int block_m,
+                                  int64_t sorted_cap);
+
+/* Zero a forward workspace (async).  A workspace must be zeroed once before
+ * its first forward; every forward returns it to the zeroed state.  Two
+ * forwards that share a workspace must not run concurrently. */
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Run the forward.  Constraints: H % 128 == 0; I % 128 == 0 (so 2I % 256 ==
+ * 0); 8 <= block_m <= 128, block_m % 8 == 0; sorted_cap >= blocks_cap *
+ * block_m; blocks_cap >= 1; a, w13, w2 and the workspace 16-byte aligned; all
+ * pointers on the current device, which must be sm_100 class or newer. */
+moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_H */

@@ -184,15 +184,19 @@ def interleave_gate_up(w13):
 
 
 def ue8m0_round_up(s):
-    """Smallest power of two >= s for s > 0 (float32); s itself when s <= 0.
+    """Smallest power of two >= s for finite s > 0 (float32); s itself otherwise.
 
     frexp gives s = f * 2**ex with f in [0.5, 1): s is a power of two exactly
-    when f == 0.5, otherwise the next power of two is 2**ex.
+    when f == 0.5, otherwise the next power of two is 2**ex.  When 2**ex is
+    not a finite float32 (s above 2**127) no rounded-up scale exists and s is
+    kept.
     """
     s = f32(s).astype(np.float64)
-    f, ex = np.frexp(s)
+    with np.errstate(invalid="ignore"):
+        f, ex = np.frexp(np.where(np.isfinite(s), s, 0.0))
     p2 = np.where(f == 0.5, s, np.exp2(ex.astype(np.float64)))
-    return f32(np.where(s > 0, p2, s))
+    p2 = np.where(p2 > np.finfo(np.float32).max, s, p2)
+    return f32(np.where((s > 0) & np.isfinite(s), p2, s))
 
 
 def requant_scales_ue8m0(codes, scale):
@@ -200,25 +204,28 @@ def requant_scales_ue8m0(codes, scale):
 
     For every block with scale s > 0: s' = 2**ceil(log2 s) and each code is
     re-encoded as E4M3(f32(decode(w) * f32(s / s'))), so that decode(w') * s'
-    stays as close as E4M3 allows to decode(w) * s.  Blocks with s == 0 are
-    left as they are.  Returns (codes', scale', ue8m0 exponent bytes) where
+    stays as close as E4M3 allows to decode(w) * s.  Blocks with s <= 0 or a
+    non-finite s are left as they are.  Returns (codes', scale', ue8m0 exponent bytes) where
     the exponent byte is log2(s') + 127 clamped to [0, 254] (0 for s == 0).
     """
     codes = np.asarray(codes, dtype=np.uint8)
     scale = f32(scale)
     E, R, C = codes.shape
+    active = (scale > 0) & np.isfinite(scale)
     s_new = ue8m0_round_up(scale)
-    ratio = np.where(scale > 0, f32(scale / np.where(s_new > 0, s_new, 1.0).astype(np.float32)), np.float32(1.0))
-    ratio = f32(ratio)
+    safe_new = np.where(active, s_new, np.float32(1.0)).astype(np.float32)
+    safe_old = np.where(active, scale, np.float32(1.0)).astype(np.float32)
+    ratio = f32(safe_old / safe_new)
     ratio_full = np.repeat(np.repeat(ratio, GROUP, axis=1), GROUP, axis=2)
     dec = f32(e4m3_decode(codes))
-    prod = f32(dec * ratio_full)
+    with np.errstate(invalid="ignore"):
+        prod = f32(dec * ratio_full)
     new_codes = e4m3_encode(prod)
-    keep = np.repeat(np.repeat(scale > 0, GROUP, axis=1), GROUP, axis=2)
+    keep = np.repeat(np.repeat(active, GROUP, axis=1), GROUP, axis=2)
     new_codes = np.where(keep, new_codes, codes).astype(np.uint8)
-    _, ex = np.frexp(s_new.astype(np.float64))
+    _, ex = np.frexp(np.where(active, s_new, 1.0).astype(np.float64))
     exp_byte = np.clip(ex - 1 + 127, 0, 254)
-    exp_byte = np.where(scale > 0, exp_byte, 0).astype(np.uint8)
+    exp_byte = np.where(active, exp_byte, 0).astype(np.uint8)
     return new_codes, s_new, exp_byte
 
 

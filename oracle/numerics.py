@@ -28,16 +28,13 @@ E4M3_MAX = 448.0
 
 def e4m3_decode(codes):
     """Decode E4M3 codes (uint8 array) to float64 values, NaN for S.1111.111."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
-    sign = (c >> 7) & 1
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int32)
     e = (c >> 3) & 0xF
     m = c & 0x7
-    sub = (m / 8.0) * 2.0 ** -6
-    nrm = (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64))
-    mag = np.where(e == 0, sub, nrm)
-    val = np.where(sign == 1, -mag, mag)
-    val = np.where((e == 15) & (m == 7), np.nan, val)
-    return val
+    # subnormal: m * 2^-9; normal: (8 + m) * 2^(e - 10)
+    mag = np.ldexp(np.where(e == 0, m, 8 + m).astype(np.float64), np.where(e == 0, -9, e - 10))
+    val = np.where((c >> 7) == 1, -mag, mag)
+    return np.where((e == 15) & (m == 7), np.nan, val)
 
 
 def e4m3_encode(x):
@@ -47,36 +44,28 @@ def e4m3_encode(x):
     (float32 inputs are exact in float64).  Within the binade
     [2**E, 2**(E+1)) the spacing of E4M3 values is 2**(E-3); below 2**-6 the
     subnormal spacing 2**-9 applies, which is the same formula with E clamped
-    to -6.  ``np.round`` rounds halves to the even integer, and an even
-    integer multiple of the spacing is an even mantissa, so this is
-    round-to-nearest-even on the E4M3 grid.
+    to -6.  So r = |x| / 2**(E-3) is exact, and ``np.round`` (halves to the
+    even integer) rounds it to the nearest representable multiple; an even r
+    is an even mantissa, so this is round-to-nearest-even on the E4M3 grid.
+    r lies in [8, 16] for normal binades (16 carries into the next binade)
+    and in [0, 8] below 2**-6.
     """
     x = np.asarray(x, dtype=np.float64)
     nan = np.isnan(x)
     neg = np.signbit(x)
     a = np.where(nan, 0.0, np.abs(x))
-    big = a > E4M3_MAX                      # includes +inf: saturates below
-    a_fin = np.where(big, E4M3_MAX, a)
-    _, ex = np.frexp(a_fin)                 # a = f * 2**ex, f in [0.5, 1)
+    a = np.minimum(a, E4M3_MAX)             # satfinite: beyond 448 (and inf) -> 448
+    _, ex = np.frexp(a)                     # a = f * 2**ex, f in [0.5, 1)
     E = np.maximum(ex - 1, -6)              # binade exponent, subnormals share -6
-    spacing = np.exp2((E - 3).astype(np.float64))
-    r = np.round(a_fin / spacing)           # exact quotient; half-to-even
-    val = r * spacing
-    val = np.minimum(val, E4M3_MAX)         # 464 rounds to 448 (tie, even) anyway
-    # bit pattern of the rounded value
-    _, ex2 = np.frexp(val)
-    is_sub = val < 2.0 ** -6
-    e_field = np.where(is_sub, 0, ex2 - 1 + 7)
-    m_field = np.where(
-        is_sub,
-        val / 2.0 ** -9,
-        val / np.exp2((ex2 - 1).astype(np.float64)) * 8.0 - 8.0,
-    )
-    e_field = np.where(val == 0, 0, e_field).astype(np.int64)
-    m_field = np.where(val == 0, 0, m_field).astype(np.int64)
-    code = (neg.astype(np.int64) << 7) | (e_field << 3) | m_field
-    code = np.where(nan, 0x7F, code)
-    return code.astype(np.uint8)
+    r = np.round(np.ldexp(a, 3 - E)).astype(np.int32)
+    carry = r == 16
+    E = E + carry
+    r = np.where(carry, 8, r)
+    normal = r >= 8
+    e_field = np.where(normal, E + 7, 0)
+    m_field = np.where(normal, r - 8, r)
+    code = (neg.astype(np.int32) << 7) | (e_field << 3) | m_field
+    return np.where(nan, 0x7F, code).astype(np.uint8)
 
 
 def bf16_round(x):

@@ -1,0 +1,115 @@
+"""The C ABI library loads and exports every symbol include/*.h declares;
+host-only entry points and host-side argument validation (no GPU needed)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from oracle import moe as oracle_moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_block_scale_gb300 import _lib
+    from fp8_block_scale_gb300.build import build
+    build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//.*", "", src)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("moe_plan", "moe_prep_weights", "moe_requant_scales_ue8m0", "moe_fp8_block_scale_forward"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    from fp8_block_scale_gb300 import moe_status_string
+    assert moe_status_string(0) == "MOE_OK"
+    assert moe_status_string(2).startswith("MOE_ERR_SHAPE")
+    assert "unknown" in moe_status_string(99)
+
+
+@pytest.mark.parametrize("M,k,E,bm", [(16, 2, 8, 64), (1, 9, 257, 64), (8192, 8, 288, 128), (4096, 10, 512, 128),
+                                      (3, 1, 1, 8)])
+def test_plan_capacity_matches_oracle(lib, M, k, E, bm):
+    from fp8_block_scale_gb300 import moe_plan_capacity
+    assert moe_plan_capacity(M, k, E, bm) == oracle_moe.plan_capacity(M, k, E, bm)
+
+
+def test_workspace_sizes(lib):
+    from fp8_block_scale_gb300 import moe_forward_workspace_size, moe_plan_workspace_size
+    ws = moe_forward_workspace_size(8192, 4096, 1024, 8, 128, 102400)
+    assert ws >= 8192 * 4096 * 4 + 102400 * 1024 + 102400 * 8 * 4
+    assert moe_plan_workspace_size(8192, 8, 288) >= 8192 * 8 * 4 + 288 * 4
+
+
+def _fake(n):
+    return ctypes.c_void_p(n)
+
+
+def test_forward_host_validation_without_gpu(lib):
+    """Argument errors are reported on the host before any device call."""
+    from fp8_block_scale_gb300._lib import MoeFwdArgs
+    f = lib.moe_fp8_block_scale_forward
+    assert f(None, None) == 1                                    # MOE_ERR_NULL
+    a = MoeFwdArgs()
+    a.M, a.H, a.I, a.E, a.top_k, a.block_m = 4, 256, 256, 8, 2, 64
+    a.sorted_cap, a.blocks_cap = 640, 10
+    a.H = 200
+    assert f(ctypes.byref(a), None) == 2                         # H % 128
+    a.H = 256
+    a.block_m = 12
+    assert f(ctypes.byref(a), None) == 2                         # block_m % 8
+    a.block_m = 256
+    assert f(ctypes.byref(a), None) == 2                         # block_m > 128
+    a.block_m = 64
+    a.sorted_cap = 639
+    assert f(ctypes.byref(a), None) == 4                         # capacity
+    a.sorted_cap = 640
+    assert f(ctypes.byref(a), None) == 1                         # null pointers
+    for name in ("a", "a_scale", "w13", "w13_scale", "w2", "w2_scale", "topk_weights", "sorted_token_ids",
+                 "expert_ids", "num_tokens_post_padded", "out", "workspace"):
+        setattr(a, name, 4096)
+    a.w13 = 4100                                                 # misaligned
+    assert f(ctypes.byref(a), None) == 3
+    a.w13 = 4096
+    a.workspace_bytes = 10
+    assert f(ctypes.byref(a), None) == 4                         # workspace too small
+    a.M = 0
+    assert f(ctypes.byref(a), None) == 0                         # nothing to do
+
+
+def test_plan_and_prep_host_validation_without_gpu(lib):
+    assert lib.moe_plan(None, 32, 4, 2, 8, 64, None, 0, None, 0, None, None, 0, None) == 1
+    p = _fake(4096)
+    assert lib.moe_plan(p, 16, 4, 2, 8, 64, p, 640, p, 10, p, p, 1 << 20, None) == 5      # id width
+    assert lib.moe_plan(p, 32, 4, 2, 8, 60, p, 640, p, 10, p, p, 1 << 20, None) == 2      # block_m
+    assert lib.moe_plan(p, 32, 4, 2, 4096, 64, p, 640, p, 10, p, p, 1 << 20, None) == 2   # E too large
+    assert lib.moe_plan(p, 32, 4, 2, 8, 64, p, 64, p, 1, p, p, 1 << 20, None) == 4        # capacity
+    assert lib.moe_prep_weights(p, p, 2, 250, 128, None) == 2
+    assert lib.moe_prep_weights(_fake(4097), p, 2, 256, 128, None) == 3
+    assert lib.moe_prep_weights(p, p, 2, 256, 128, None) == 2                             # overlap
+    assert lib.moe_requant_scales_ue8m0(p, p, None, 1, 100, 128, None) == 2
+    assert lib.moe_quantize_act_1x128(p, 4, 100, p, p, None) == 2
+    assert lib.moe_quantize_weight_128x128(p, 1, 128, 64, p, p, None) == 2

@@ -1,0 +1,201 @@
+"""GPU parity of moe_fp8_block_scale_forward against the oracle.
+
+Small problems are compared on every token; the full-size workloads (in the
+launch configuration the benchmark times) on a deterministic token sample,
+which the oracle evaluates exactly because tokens are independent.  Both the
+output and the requantised intermediate codes are checked.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from fp8_block_scale_gb300 import _lib as L
+from fp8_block_scale_gb300 import workloads as W
+from fp8_block_scale_gb300.problem import DeviceProblem
+from oracle import moe as O
+from tests.moe_ref import CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, oracle_inputs, out_metrics
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _load():
+    L.load()
+
+
+def _run(prob, debug=True):
+    cap = prob.sorted_ids.numel()
+    dq = torch.zeros(cap, prob.cfg.I, dtype=torch.uint8, device="cuda") if debug else None
+    ds = torch.zeros(cap, prob.cfg.I // 128, dtype=torch.float32, device="cuda") if debug else None
+    prob.run_plan()
+    prob.run_forward(prob.fwd_args(dq, ds))
+    torch.cuda.synchronize()
+    return dq, ds
+
+
+def _check(prob, tokens, dq=None, ds=None, label=""):
+    cfg = prob.cfg
+    inp, experts = oracle_inputs(cfg, prob.routing, tokens)
+    # the GPU quantisers saw the same raw values: their codes must match bit for bit
+    for i, e in enumerate(experts[:4]):
+        assert np.array_equal(prob.w13_logical[e].cpu().numpy(), inp["w13_q"][i]), f"W13 codes of expert {e}"
+        assert np.array_equal(prob.w13_scale[e].cpu().numpy().view(np.uint32), inp["w13_s"][i].view(np.uint32))
+        assert np.array_equal(prob.w2[e].cpu().numpy(), inp["w2_q"][i])
+    ref, inter = O.moe_forward(**inp, routed_scale=cfg.routed_scale, return_inter=True)
+    got = prob.out[torch.as_tensor(tokens, device="cuda")].float().cpu().numpy()
+    m = out_metrics(got, ref, inp["out_prior"])
+    print(f"{label} {cfg.name} tokens={len(tokens)} {m}")
+    assert m["rel_l2"] <= REL_L2_TOL, m
+    assert m["max_rel"] <= MAX_ABS_TOL, m
+    if dq is not None:
+        sorted_ids = prob.sorted_ids.cpu().numpy()
+        P = int(prob.ntpp.item())
+        slot_of = {int(r): s for s, r in enumerate(sorted_ids[:P]) if r < cfg.R}
+        dqn = dq.cpu().numpy()
+        dsn = ds.cpu().numpy()
+        n_codes = n_diff = n_far = 0
+        for (ti, j), (codes, scales) in inter.items():
+            r = int(tokens[ti]) * cfg.top_k + j
+            s = slot_of[r]
+            nd, nf = code_diffs(dqn[s], codes)
+            n_codes += codes.size
+            n_diff += nd
+            n_far += nf
+            np.testing.assert_allclose(dsn[s], scales, rtol=1e-5, atol=0)
+        print(f"   intermediate codes: {n_diff}/{n_codes} differ, {n_far} not adjacent")
+        assert n_far == 0
+        assert n_diff <= max(1, CODE_DIFF_FRAC * n_codes)
+    return m
+
+
+# ------------------------------------------------------------------ small problems, every token
+
+SMALL = {
+    "tiny": W.CONFIGS["tiny"],
+    "ragged_bm8": W.MoEConfig("ragged_bm8", M=37, H=384, I=256, E=5, top_k=3, block_m=8, out_init="normal0.1"),
+    "ragged_bm64": W.MoEConfig("ragged_bm64", M=37, H=384, I=256, E=5, top_k=3, block_m=64, routed_scale=2.5,
+                               id_dtype=torch.int64),
+    "ragged_bm128": W.MoEConfig("ragged_bm128", M=200, H=256, I=384, E=3, top_k=2, block_m=128,
+                                out_init="normal0.1"),
+    "masked_zero": W.MoEConfig("masked_zero", M=61, H=512, I=256, E=9, top_k=4, block_m=64, routing="skewed",
+                               masked_frac=0.1, n_hot=2, hot_frac=0.5, n_zero_scale=2),
+    "hot_many_blocks": W.MoEConfig("hot_many_blocks", M=500, H=256, I=256, E=6, top_k=2, block_m=64,
+                                   routing="skewed", n_hot=1, hot_frac=0.9),
+    "ue8m0_small": W.MoEConfig("ue8m0_small", M=40, H=384, I=128, E=4, top_k=2, block_m=64, ue8m0=True,
+                               out_init="normal0.1"),
+    "h_odd_tiles": W.MoEConfig("h_odd_tiles", M=20, H=640, I=128, E=3, top_k=2, block_m=32),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small_all_tokens(name):
+    prob = DeviceProblem(SMALL[name])
+    dq, ds = _run(prob)
+    _check(prob, np.arange(prob.cfg.M), dq, ds, "small")
+    assert int(prob.status.item()) == 0
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled tokens
+
+FULL = {
+    "decode_m1": None, "decode_m8": None, "decode_m64": 6,
+    "prefill_1024": 3, "prefill_2048": 2, "prefill_4096": 2, "prefill_8192": 2,
+    "skewed": 3, "large": 2,
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_forward_full_size_sampled(name):
+    cfg = W.CONFIGS[name]
+    prob = DeviceProblem(cfg)
+    dq, ds = _run(prob)
+    n = FULL[name]
+    if n is None:
+        tokens = np.arange(cfg.M)
+    else:
+        tokens = np.unique(np.linspace(0, cfg.M - 1, n).astype(np.int64))
+    if name == "skewed":
+        ids = prob.routing.topk_ids.numpy()
+        z = prob.routing.zero_scale_experts[0]
+        masked = np.nonzero((ids == -1).any(axis=1))[0]
+        zero = np.nonzero((ids == z).any(axis=1))[0]
+        tokens = np.unique(np.concatenate([tokens, masked[:1], zero[:1]]))
+    _check(prob, tokens, dq, ds, "full")
+    assert int(prob.status.item()) == 0
+
+
+# ------------------------------------------------------------------ semantics
+
+def test_forward_accumulates_and_leaves_workspace_zeroed():
+    cfg = SMALL["ragged_bm64"]
+    prob = DeviceProblem(cfg)
+    _run(prob, debug=False)
+    once = prob.out.float().clone()
+    prob.run_forward()
+    torch.cuda.synchronize()
+    twice = prob.out.float()
+    acc_bytes = cfg.M * cfg.H * 4
+    assert int(prob.workspace[:acc_bytes].view(torch.int32).abs().sum().item()) == 0
+    delta1 = once - prob.out_prior.float()
+    delta2 = twice - once
+    rel = (delta2 - delta1).norm() / delta1.norm()
+    assert rel < 2e-2, rel.item()
+
+
+def test_forward_all_masked_leaves_out_unchanged():
+    cfg = SMALL["tiny"].with_(name="all_masked", masked_frac=1.0)
+    prob = DeviceProblem(cfg)
+    assert (prob.routing.topk_ids == -1).all()
+    _run(prob, debug=False)
+    assert torch.equal(prob.out.view(torch.int16), prob.out_prior.view(torch.int16))
+    assert int(prob.ntpp.item()) == 0
+
+
+def test_forward_truncated_extent_only_counts_leading_blocks():
+    """Blocks at and past num_tokens_post_padded exit untouched."""
+    cfg = SMALL["ragged_bm64"]
+    prob = DeviceProblem(cfg)
+    prob.run_plan()
+    torch.cuda.synchronize()
+    bm = cfg.block_m
+    sorted_ids = prob.sorted_ids.cpu().numpy()
+    kept = set(int(r) for r in sorted_ids[:bm] if r < cfg.R)
+    prob.ntpp.fill_(bm)
+    prob.run_forward()
+    torch.cuda.synchronize()
+    ids = prob.routing.topk_ids.to(torch.int64).numpy().copy()
+    flat = ids.reshape(-1)
+    for r in range(flat.size):
+        if r not in kept:
+            flat[r] = -1
+    routing = W.Routing(torch.from_numpy(ids), prob.routing.topk_weights, prob.routing.zero_scale_experts)
+    tokens = np.arange(cfg.M)
+    inp, _ = oracle_inputs(cfg, routing, tokens)
+    ref = O.moe_forward(**inp, routed_scale=cfg.routed_scale)
+    m = out_metrics(prob.out.float().cpu().numpy(), ref)
+    assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, m
+
+
+def test_forward_reports_bad_expert_in_plan():
+    cfg = SMALL["tiny"]
+    prob = DeviceProblem(cfg)
+    prob.run_plan()
+    torch.cuda.synchronize()
+    prob.expert_ids[0] = cfg.E + 3                         # corrupt one block of the plan
+    prob.run_forward()
+    torch.cuda.synchronize()
+    assert int(prob.status.item()) & L.MOE_DEV_BAD_EXPERT
+    assert torch.isfinite(prob.out.float()).all()
+
+
+def test_forward_rejects_pointer_on_host():
+    cfg = SMALL["tiny"]
+    prob = DeviceProblem(cfg)
+    prob.run_plan()
+    args = prob.fwd_args()
+    host = torch.zeros(cfg.M, cfg.top_k, dtype=torch.float32)
+    args.topk_weights = host.data_ptr()
+    with pytest.raises(L.MoeError) as ei:
+        prob.run_forward(args)
+    assert ei.value.status == 6
