@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Benchmark of the fused block-scaled FP8 MoE path on GB300.
+
+One step = one pass of the hot path over one batch: the routing plan
+(moe_plan) and the fused forward (moe_fp8_block_scale_forward: gate/up GEMM +
+SwiGLU + requant, down GEMM + route reduce, BF16 finalize), on the prefill
+workload E288/H4096/I1024/top-8 at 8192 tokens, inputs resident in HBM.
+L2 is flushed (a write larger than L2) between timed steps, outside the
+timed intervals, and each step is timed with CUDA events on its stream.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded token sample of the same workload instead.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused FP8 MoE ms/call & TFLOPS (E288 H4096 I1024 top8, 1K-8K tok), % roofline"
+UNIT = "TFLOP/s"
+HEADLINE = "prefill_8192"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def work(cfg, topk_ids):
+    """Algorithmic FLOPs and bytes of one step (valid routes only, touched experts only)."""
+    import numpy as np
+    ids = np.asarray(topk_ids).astype(np.int64).reshape(-1)
+    valid = ids[(ids >= 0) & (ids < cfg.E)]
+    Rv = int(valid.size)
+    U = int(np.unique(valid).size)
+    M, H, I, R = cfg.M, cfg.H, cfg.I, cfg.R
+    w13_b = 2 * I * H + 4 * (2 * I // 128) * (H // 128)
+    w2_b = H * I + 4 * (H // 128) * (I // 128)
+    act_b = M * H + 4 * M * (H // 128)
+    inter_b = Rv * (I + 4 * (I // 128))
+    up = {"flop": Rv * 4 * H * I, "bytes": U * w13_b + act_b + inter_b}
+    down = {"flop": Rv * 2 * H * I, "bytes": U * w2_b + inter_b + 4 * M * H + 4 * R}
+    total = {"flop": Rv * 6 * H * I,
+             "bytes": U * (w13_b + w2_b) + act_b + 4 * M * H + 8 * R}
+    return {"Rv": Rv, "U": U, "up": up, "down": down, "total": total}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("forward.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "fp8_block_scale_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    matches the kernel source; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+        rec = t[kernel][workload]
+        if rec.get("source_hash") != kernel_source_hash():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def time_steps(prob, steps, warmup, flush, with_kernel_events=True):
+    """Per-step CUDA-event times (ms) of plan + forward; per-kernel times of the forward."""
+    import torch
+    from fp8_block_scale_gb300 import _lib as L
+
+    stream = torch.cuda.current_stream()
+    args = prob.fwd_args()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for evs in kev:
+        for e in evs:
+            e.record(stream)          # creates the underlying cudaEvent
+    argsets = []
+    for i in range(steps):
+        a = prob.fwd_args()
+        if with_kernel_events:
+            L.set_profile_events(a, kev[i])
+        argsets.append(a)
+    for _ in range(warmup):
+        flush.zero_()
+        prob.run_plan()
+        prob.run_forward(args)
+    torch.cuda.synchronize()
+    return starts, ends, kev, argsets
+
+
+def run_timed(prob, steps, starts, ends, argsets, flush):
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        prob.run_plan()
+        prob.run_forward(argsets[i])
+        ends[i].record()
+
+
+def measure(prob, steps, warmup, flush, dist=None, clocks=None):
+    import torch
+    starts, ends, kev, argsets = time_steps(prob, steps, warmup, flush)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    t0 = time.perf_counter()
+    run_timed(prob, steps, starts, ends, argsets, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    up_ms = [k[0].elapsed_time(k[1]) for k in kev]
+    dn_ms = [k[1].elapsed_time(k[2]) for k in kev]
+    fin_ms = [k[2].elapsed_time(k[3]) for k in kev]
+    plan_ms = [s.elapsed_time(k[0]) for s, k in zip(starts, kev)]
+    return {"step_ms": statistics.mean(step_ms), "step_ms_median": statistics.median(step_ms),
+            "up_ms": statistics.mean(up_ms), "down_ms": statistics.mean(dn_ms), "finalize_ms": statistics.mean(fin_ms),
+            "plan_ms": statistics.mean(plan_ms), "forward_ms": statistics.mean(u + d + f for u, d, f in
+                                                                              zip(up_ms, dn_ms, fin_ms)),
+            "wall_s": wall, "clocks": clk}
+
+
+def measure_e2e(prob, steps, warmup):
+    """Same step through the public API with host buffers: H2D of the step's
+    inputs from pinned memory, plan, forward, D2H of the output."""
+    import torch
+    cfg = prob.cfg
+    host = {
+        "a": prob.a.cpu().pin_memory(), "a_scale": prob.a_scale.cpu().pin_memory(),
+        "topk_ids": prob.topk_ids.cpu().pin_memory(), "topk_weights": prob.topk_weights.cpu().pin_memory(),
+        "out": prob.out_prior.cpu().pin_memory(),
+    }
+    out_h = torch.empty_like(host["out"]).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    args = prob.fwd_args()
+
+    def step():
+        prob.a.copy_(host["a"], non_blocking=True)
+        prob.a_scale.copy_(host["a_scale"], non_blocking=True)
+        prob.topk_ids.copy_(host["topk_ids"], non_blocking=True)
+        prob.topk_weights.copy_(host["topk_weights"], non_blocking=True)
+        prob.out.copy_(host["out"], non_blocking=True)
+        prob.run_plan()
+        prob.run_forward(args)
+        out_h.copy_(prob.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------- oracle timing (CPU baseline)
+
+def _oracle_child(npz_path, groups_json):
+    """Runs in a fresh process with one BLAS/OpenMP thread: times the oracle
+    forward on each group of (local) token indices, one timing per group."""
+    import numpy as np
+    from oracle import moe as O
+    d = dict(np.load(npz_path))
+    rs = float(d.pop("routed_scale"))
+    secs = []
+    for g in json.loads(groups_json):
+        t0 = time.perf_counter()
+        O.moe_forward(**d, routed_scale=rs, tokens=g)
+        secs.append(time.perf_counter() - t0)
+    print(json.dumps({"seconds": secs}))
+
+
+def oracle_sample_seconds(cfg, routing, tokens, groups):
+    """Oracle inputs for the token sample (built here, untimed), then the oracle
+    forward timed per group of sample positions in a single-threaded child."""
+    import numpy as np
+    from oracle.inputs import oracle_inputs
+    inp, _ = oracle_inputs(cfg, routing, tokens)
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, routed_scale=np.float32(cfg.routed_scale), **inp)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", path, json.dumps(groups)],
+                       env=env, capture_output=True, text=True, cwd=ROOT)
+    os.unlink(path)
+    if r.returncode != 0:
+        raise RuntimeError("oracle child failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])["seconds"]
+
+
+def sample_tokens(cfg, n, offset=0):
+    import numpy as np
+    return np.unique((np.linspace(0, cfg.M - 1, n).astype(np.int64) + offset) % cfg.M)
+
+
+def _valid_routes(cfg, routing, tokens):
+    import torch
+    ids = routing.topk_ids.to(torch.int64).numpy()[tokens]
+    return int(((ids >= 0) & (ids < cfg.E)).sum())
+
+
+def cpu_baseline(cfg, routing, n_tokens=4):
+    tokens = sample_tokens(cfg, n_tokens)
+    secs = sum(oracle_sample_seconds(cfg, routing, tokens, [list(range(len(tokens)))]))
+    rv = _valid_routes(cfg, routing, tokens)
+    flop = rv * 6 * cfg.H * cfg.I
+    return {"value": flop / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(tokens)} of {cfg.M} tokens ({rv} routes) of {cfg.name}, oracle forward only, "
+                      f"one BLAS thread, {secs:.1f} s"}
+
+
+# ---------------------------------------------------------------- main
+
+def workload_desc(cfg):
+    return (f"{cfg.name}: M={cfg.M} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.top_k} block_m={cfg.block_m}, "
+            f"{cfg.routing} routing")
+
+
+def run_reference(args, rank):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample:
+    each step is one token (all of its routes) of the workload."""
+    from fp8_block_scale_gb300 import workloads as W
+    if rank != 0:
+        return
+    cfg = W.CONFIGS[args.workload]
+    routing = W.make_routing(cfg)
+    n = args.warmup + args.steps
+    pool = sample_tokens(cfg, min(n, 4))
+    groups = [[i % len(pool)] for i in range(n)]
+    secs = oracle_sample_seconds(cfg, routing, pool, groups)[args.warmup:]
+    flops = [_valid_routes(cfg, routing, pool[g]) * 6 * cfg.H * cfg.I for g in groups[args.warmup:]]
+    value = sum(flops) / sum(secs) / 1e12
+    ms = 1e3 * sum(secs) / len(secs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (numpy oracle)", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "sample": "1 token per step (all its routes)",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"1 token of {cfg.M} per step, {args.steps} steps, one BLAS thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    from fp8_block_scale_gb300 import _lib as L
+    from fp8_block_scale_gb300 import workloads as W
+    from fp8_block_scale_gb300.problem import DeviceProblem
+
+    L.load()
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    cfg = W.CONFIGS[args.workload]
+    prob = DeviceProblem(cfg)
+    w = work(cfg, prob.routing.topk_ids.to(torch.int64).numpy())
+    res = measure(prob, args.steps, args.warmup, flush, dist, ClockSampler(dev) if rank == 0 else None)
+
+    # max over ranks of the timed interval
+    step_ms = res["step_ms"]
+    if dist is not None:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    total_flop = w["total"]["flop"] * world
+    value = total_flop / (step_ms * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = (float("nan"), 0, 0) if args.no_e2e else measure_e2e(prob, max(3, args.steps // 2), 2)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return
+
+    fp8_peak = 2.0 * peaks["bf16_tflops"]          # FP8 dense = 2x BF16 dense (nominal 4.5 / 2.25 PF)
+    hbm = peaks["hbm_gbs"]
+    # dominant kernel: the gate/up GEMM
+    up_s = res["up_ms"] * 1e-3
+    t_up_bytes = w["up"]["bytes"] / (hbm * 1e9)
+    t_up_flop = w["up"]["flop"] / (fp8_peak * 1e12)
+    if t_up_bytes >= t_up_flop:
+        achieved = w["up"]["bytes"] / up_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+    else:
+        achieved = w["up"]["flop"] / up_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak}
+    roof["traffic"] = recorded_traffic("moe_gemm_kernel<up>", cfg.name)
+    roof["kernel"] = "moe_gemm_kernel<up> (gate/up GEMM + SwiGLU + requant)"
+    roof["peak_source"] = (f"{peaks['source']} (hbm_gbs; fp8 = 2 x bf16_tflops {peaks['bf16_tflops']})")
+    roof["algorithmic_per_launch"] = {"bytes": w["up"]["bytes"], "flop": w["up"]["flop"]}
+    t_roof = max(w["total"]["flop"] / (fp8_peak * 1e12), w["total"]["bytes"] / (hbm * 1e9))
+
+    clocks = res["clocks"] or {}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "step": "moe_plan + moe_fp8_block_scale_forward",
+                   "l2": "flushed between steps (2 x L2 write), per-step CUDA events",
+                   "parallelism": f"replicas x{world} (tokens independent, no collective)"},
+        "roofline": roof,
+        "ms_forward": res["forward_ms"], "ms_plan": res["plan_ms"],
+        "ms_kernels": {"up": res["up_ms"], "down": res["down_ms"], "finalize": res["finalize_ms"]},
+        "tflops_forward": w["total"]["flop"] / (res["forward_ms"] * 1e-3) / 1e12,
+        "roofline_step": {"t_flop_us": w["total"]["flop"] / (fp8_peak * 1e12) * 1e6,
+                          "t_bytes_us": w["total"]["bytes"] / (hbm * 1e9) * 1e6,
+                          "frac_forward": t_roof / (res["forward_ms"] * 1e-3),
+                          "frac_step": t_roof / (step_ms * 1e-3)},
+        "gpu_launches": 6 * args.steps,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons", [])},
+        "e2e": {"value": w["total"]["flop"] * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    if not args.no_extra:
+        line["sweep"] = extra_sweep(cfg, prob, flush, peaks)
+    del prob
+    torch.cuda.empty_cache()
+    try:
+        if args.no_cpu_baseline:
+            raise RuntimeError("skipped (--no-cpu-baseline)")
+        line["cpu_baseline"] = cpu_baseline(cfg, W.make_routing(cfg), n_tokens=args.oracle_tokens)
+    except Exception as ex:  # the baseline must not hide the measurement
+        line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {ex}"}
+    print(json.dumps(line), flush=True)
+
+
+def extra_sweep(cfg, prob, flush, peaks):
+    """Other token counts of the same weights, and the decode workload."""
+    import torch
+    from fp8_block_scale_gb300 import workloads as W
+    from fp8_block_scale_gb300.problem import DeviceProblem
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    for name in ("prefill_1024", "prefill_2048", "prefill_4096"):
+        c = W.CONFIGS[name]
+        p = DeviceProblem(c, weights_from=prob)
+        r = measure(p, 10, 3, flush)
+        w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
+        t_roof = max(w["total"]["flop"] / (fp8_peak * 1e12), w["total"]["bytes"] / (hbm * 1e9))
+        out[name] = {"ms_forward": r["forward_ms"], "ms_step": r["step_ms"],
+                     "tflops_forward": w["total"]["flop"] / (r["forward_ms"] * 1e-3) / 1e12,
+                     "frac_roofline_forward": t_roof / (r["forward_ms"] * 1e-3)}
+        del p
+    base = None
+    for name in ("decode_m1", "decode_m8", "decode_m64"):
+        c = W.CONFIGS[name]
+        p = DeviceProblem(c, weights_from=base)
+        base = base or p
+        r = measure(p, 20, 5, flush)
+        w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
+        gbs = w["total"]["bytes"] / (r["forward_ms"] * 1e-3) / 1e9
+        out[name] = {"ms_forward": r["forward_ms"], "ms_step": r["step_ms"], "gbs_forward": gbs,
+                     "frac_hbm_forward": gbs / hbm, "ms_kernels": {"up": r["up_ms"], "down": r["down_ms"],
+                                                                   "finalize": r["finalize_ms"]}}
+    del base
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="skip the sweep of other token counts")
+    ap.add_argument("--oracle-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing (profiling runs)")
+    ap.add_argument("--oracle-child", nargs=2, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_child:
+        _oracle_child(*args.oracle_child)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            tdist.init_process_group("nccl")
+        else:
+            tdist.init_process_group("gloo")
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank)
+        else:
+            run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -57,6 +57,7 @@ class MoeFwdArgs(ctypes.Structure):
         ("top_k", ctypes.c_int32),
         ("block_m", ctypes.c_int32),
         ("routed_scale", ctypes.c_float),
+        ("profile_events", ctypes.POINTER(ctypes.c_void_p)),
     ]
 
 
@@ -198,6 +199,17 @@ def make_fwd_args(a, a_scale, w13, w13_scale, w2, w2_scale, topk_weights, sorted
     args.top_k, args.block_m = top_k, block_m
     args.routed_scale = routed_scale
     return args
+
+
+def set_profile_events(args, events):
+    """Attach 4 recorded torch.cuda.Event objects (or None) to a moe_fwd_args."""
+    if events is None:
+        args.profile_events = None
+        args._events_keepalive = None
+        return
+    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    args._events_keepalive = arr
+    args.profile_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
 
 
 def moe_fp8_block_scale_forward(args, stream=None):

@@ -501,6 +501,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   p.H = a->H;
   p.routed_scale = a->routed_scale;
 
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
+  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
   if (nblocks > 0) {
     GemmParams up = p;
     up.a_scale = a->a_scale;
@@ -517,6 +519,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
     moe_gemm_kernel<true><<<up_grid, kNumThreads, kSmemBytes, stream>>>(tm_a, tm_w13, up);
     MOE_CUDA_TRY(cudaGetLastError());
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
 
     GemmParams dn = p;
     dn.a_scale = s_inter;
@@ -531,13 +534,17 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     const int dn_grid = static_cast<int>(dn_tiles < dev.sms ? dn_tiles : dev.sms);
     moe_gemm_kernel<false><<<dn_grid, kNumThreads, kSmemBytes, stream>>>(tm_q, tm_w2, dn);
     MOE_CUDA_TRY(cudaGetLastError());
+  } else if (ev) {
+    MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
   }
+  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[2], stream));
 
   const int64_t n8 = a->M * a->H / 8;
   int64_t fgrid = ceil_div(n8, 256);
   if (fgrid > static_cast<int64_t>(dev.sms) * 8) fgrid = static_cast<int64_t>(dev.sms) * 8;
   finalize_kernel<<<static_cast<unsigned>(fgrid), 256, 0, stream>>>(a->out, acc, n8);
   MOE_CUDA_TRY(cudaGetLastError());
+  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
   return MOE_OK;
 }
 

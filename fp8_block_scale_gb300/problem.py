@@ -14,7 +14,14 @@ from . import workloads as W
 
 
 class DeviceProblem:
-    def __init__(self, cfg: W.MoEConfig, device="cuda", chunk_experts=16, worst_case_plan=None):
+    """Quantised inputs, prepared weights, plan buffers and workspace of a workload.
+
+    ``weights_from`` reuses the prepared weights of another problem with the
+    same H, I, E, seed and weight options (a sweep over token counts).
+    """
+
+    def __init__(self, cfg: W.MoEConfig, device="cuda", chunk_experts=16, worst_case_plan=None,
+                 weights_from=None):
         self.cfg = cfg
         self.device = device
         dev = torch.device(device)
@@ -28,6 +35,18 @@ class DeviceProblem:
         L.moe_quantize_act_1x128(x, self.a, self.a_scale)
         del x
 
+        if weights_from is not None:
+            src = weights_from
+            assert (src.cfg.H, src.cfg.I, src.cfg.E, src.cfg.seed, src.cfg.ue8m0) == (H, I, E, cfg.seed, cfg.ue8m0)
+            self.w13_logical, self.w13_scale, self.w2, self.w2_scale, self.w13 = (
+                src.w13_logical, src.w13_scale, src.w2, src.w2_scale, src.w13)
+        else:
+            self._make_weights(cfg, dev, chunk_experts)
+        self._make_rest(cfg, dev, worst_case_plan)
+
+    def _make_weights(self, cfg, dev, chunk_experts):
+        H, I, E = cfg.H, cfg.I, cfg.E
+        N = 2 * I
         self.w13_logical = torch.empty(E, N, H, dtype=torch.uint8, device=dev)
         self.w13_scale = torch.empty(E, N // 128, H // 128, dtype=torch.float32, device=dev)
         self.w2 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
@@ -47,6 +66,9 @@ class DeviceProblem:
             L.moe_requant_scales_ue8m0(self.w2, self.w2_scale)
         self.w13 = torch.empty_like(self.w13_logical)
         L.moe_prep_weights(self.w13_logical, self.w13)
+
+    def _make_rest(self, cfg, dev, worst_case_plan):
+        M, H, I, E, k, bm = cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k, cfg.block_m
 
         self.topk_ids = self.routing.topk_ids.to(dev)
         self.topk_weights = self.routing.topk_weights.to(dev)

@@ -110,7 +110,8 @@ moe_status moe_prep_weights(const uint8_t* w13, uint8_t* w13_interleaved,
  * powers of two).  For every 128x128 block with FP32 scale s > 0:
  * s' = 2^ceil(log2 s) (rounded up) and every code w becomes
  * E4M3_rn_satfinite(f32(decode(w) * f32(s / s'))).  Blocks with s <= 0 or a
- * non-finite s are left unchanged.
+ * non-finite s are left unchanged, and so is a scale above 2^127 that is not a
+ * power of two (no FP32 power of two lies above it).
  *  w          [E, rows, cols] E4M3 codes, rewritten in place
  *  scale      [E, rows/128, cols/128] FP32, rewritten in place
  *  ue8m0_exp  nullable [E, rows/128, cols/128] uint8 out: log2(s') + 127
@@ -178,6 +179,10 @@ typedef struct moe_fwd_args {
   int32_t top_k;
   int32_t block_m;
   float routed_scale;                      /* routed scaling factor (1.0 = none)            */
+  void* const* profile_events;             /* nullable: 4 cudaEvent_t handles, recorded on
+                                              `stream` before the gate/up kernel, after it,
+                                              after the down kernel and after the finalize
+                                              kernel (per-kernel timing; no effect if NULL)  */
 } moe_fwd_args;
 
 /* Workspace bytes the forward needs (host-only).  The workspace holds the

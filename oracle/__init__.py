@@ -25,6 +25,8 @@ Modules:
   definitions.
 * ``moe`` -- quantisers, routing plan, gate/up interleave, UE8M0 requant, the
   forward pass (FP32 emulation) and an FP64 twin used to pin it.
+* ``inputs`` -- oracle-side inputs regenerated from the seeded workload
+  generator, and the parity metrics (tolerances of the forward).
 
 Pinning status: every function here is pinned by a CPU test under
 ``tests/`` (exhaustive codec checks, closed forms, brute force on tiny inputs,
@@ -33,4 +35,4 @@ print no worked numeric example, so no value in the oracle is pinned to a
 number printed on the pages.
 """
 
-from . import numerics, moe  # noqa: F401
+from . import numerics, moe  # noqa: F401  (``inputs`` needs torch: import it explicitly)

@@ -1,16 +1,17 @@
-"""Test helpers: oracle-side inputs and comparison metrics for GPU parity tests.
+"""Oracle-side inputs of a workload, and the comparison metrics.
 
-The oracle never sees a value produced by the CUDA library: its inputs are
-the raw BF16 values regenerated from the seeded generator and quantised by
-the oracle's own quantiser.
+TEST INFRASTRUCTURE ONLY (see the package docstring).  The oracle never sees
+a value produced by the CUDA library: its inputs are the raw BF16 values
+regenerated from the seeded generator module (which holds none of the
+method's arithmetic) and quantised by the oracle's own quantiser.
 """
 
 import numpy as np
 import torch
 
 from fp8_block_scale_gb300 import workloads as W
-from oracle import moe as O
-from oracle.numerics import e4m3_decode
+from . import moe as O
+from .numerics import e4m3_decode
 
 # The numerical acceptance bar of the forward: relative L2 error of `out`,
 # max |diff| relative to max |ref|, and the intermediate FP8 codes: at most
@@ -22,8 +23,14 @@ CODE_DIFF_FRAC = 1e-3
 _E4M3_SORTED = np.unique(np.abs(e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))))
 
 
-def oracle_inputs(cfg, routing, tokens, device="cuda"):
-    """Oracle inputs for `tokens`: a compact problem over the experts they touch."""
+def oracle_inputs(cfg, routing, tokens, device=None):
+    """Oracle inputs for `tokens`: a compact problem over the experts they touch.
+
+    Raw values are drawn on `device` (CUDA when available, as the GPU side
+    draws them, else CPU) and copied to the host before quantisation.
+    """
+    if device is None:
+        device = "cuda" if torch.cuda.is_available() else "cpu"
     tokens = np.asarray(tokens, dtype=np.int64)
     ids = routing.topk_ids.to(torch.int64).numpy()[tokens]
     experts = sorted({int(e) for e in ids.reshape(-1) if 0 <= e < cfg.E})

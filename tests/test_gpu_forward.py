@@ -14,7 +14,7 @@ from fp8_block_scale_gb300 import _lib as L
 from fp8_block_scale_gb300 import workloads as W
 from fp8_block_scale_gb300.problem import DeviceProblem
 from oracle import moe as O
-from tests.moe_ref import CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, oracle_inputs, out_metrics
+from oracle.inputs import CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, oracle_inputs, out_metrics
 
 pytestmark = pytest.mark.gpu
 
