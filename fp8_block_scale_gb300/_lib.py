@@ -83,6 +83,8 @@ _SIGS = {
                                                      ctypes.c_int, ctypes.c_int64]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_fp8_block_scale_forward": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
+    "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "moe_fp8_block_scale_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
 }
 
 
@@ -214,3 +216,13 @@ def set_profile_events(args, events):
 
 def moe_fp8_block_scale_forward(args, stream=None):
     _check("moe_fp8_block_scale_forward", load().moe_fp8_block_scale_forward(ctypes.byref(args), _stream(stream)))
+
+
+def moe_noalloc_scratch_bytes():
+    return load().moe_noalloc_scratch_bytes()
+
+
+def moe_fp8_block_scale_forward_noalloc(args, stream=None):
+    """Forward without a caller workspace (static device scratch; see the header)."""
+    _check("moe_fp8_block_scale_forward_noalloc",
+           load().moe_fp8_block_scale_forward_noalloc(ctypes.byref(args), _stream(stream)))

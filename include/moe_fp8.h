@@ -202,6 +202,32 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_strea
  * pointers on the current device, which must be sm_100 class or newer. */
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free forward.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot call cudaMalloc: engines that
+ * hand all of device memory to their own pool at start-up and forbid any
+ * later allocation, plug-ins that reach the GPU only through this C ABI and
+ * own no allocator, and latency-critical loops where an allocation could
+ * synchronise the device.
+ *
+ * Same arguments and results as moe_fp8_block_scale_forward, except that
+ * args->workspace and args->workspace_bytes are ignored: the scratch is a
+ * file-scope static device array of moe_noalloc_scratch_bytes() bytes
+ * (32 MiB) that every GPU loading the library holds until the process exits.
+ * Problems whose moe_forward_workspace_size exceeds it are rejected with
+ * MOE_ERR_CAPACITY before anything is launched (decode-sized problems fit;
+ * prefill-sized ones do not).  The caller still passes every input and the
+ * output.  Each call zeroes the part of the array it uses (async, on
+ * `stream`) before the forward.  All calls share the one array, so calls
+ * whose work overlaps on the GPU (different streams, or different host
+ * threads) race and corrupt each other's results: serialise them.  The first
+ * call on a device looks up the array's device address for that device (a
+ * host-side set-up step); make that first call before any stream capture.
+ * Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
+ * ------------------------------------------------------------------------ */
+size_t moe_noalloc_scratch_bytes(void);
+moe_status moe_fp8_block_scale_forward_noalloc(const moe_fwd_args* args, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
