@@ -80,7 +80,7 @@ _SIGS = {
     "moe_quantize_weight_128x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_forward_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                     ctypes.c_int, ctypes.c_int64]),
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_fp8_block_scale_forward": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
     "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -165,8 +165,8 @@ def moe_quantize_weight_128x128(w_bf16, q, scale, stream=None):
         _ptr(w_bf16), E, rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
 
 
-def moe_forward_workspace_size(M, H, I, top_k, block_m, sorted_cap):
-    return load().moe_forward_workspace_size(M, H, I, top_k, block_m, sorted_cap)
+def moe_forward_workspace_size(M, H, I, E, top_k, block_m, sorted_cap):
+    return load().moe_forward_workspace_size(M, H, I, E, top_k, block_m, sorted_cap)
 
 
 def moe_workspace_init(workspace, stream=None):

@@ -3,9 +3,14 @@
 // and review fixes"; post-dot scale application from "Final W8 kernel
 // performance (v46)").
 //
-// Three launches on the caller's stream:
+// Launches on the caller's stream:
+//   0. stage: per plan slot, the route's token and weight and the activation
+//      block scales (transposed, one row per K slice); per (plan block,
+//      n tile, K slice) a 16-byte record of the two weight block scales the
+//      tile needs; for well-filled plans also the activation rows themselves,
+//      in plan order.  Everything the GEMM epilogues need thus arrives by TMA.
 //   1. up   (gemm kernel, kUp = true): for every (plan block, 256-wide tile of
-//      the interleaved gate/up weights): gathered activation rows x W13 tile on
+//      the interleaved gate/up weights): activation rows x W13 tile on
 //      tcgen05 tensor cores, one 128-wide K slice at a time into TMEM; the
 //      epilogue warps promote each slice in FP32 with the activation and
 //      weight block scales, then apply SwiGLU and requantise the 128
@@ -17,17 +22,20 @@
 //   3. finalize: out = bf16_rn(f32(out) + acc); acc = 0.
 //
 // The GEMM kernel is persistent and warp specialised (320 threads):
-//   warp 0      TMA producer: gathered activation rows (tile::gather4) or
-//               intermediate rows, plus the 256-row weight tile, into a
-//               4-stage ring of 48 KiB stages (128-byte swizzle);
+//   warp 0      TMA producer: activation (or intermediate) rows, the 256-row
+//               weight tile and the slice's scales into a 4-stage ring;
 //   warp 1      TMEM allocation and the single MMA-issuing thread
 //               (kind::f8f6f4, M=128, N=256, K=32 per instruction, 4 per slice);
 //   warps 2..9  epilogue: each owns 32 tile rows (its TMEM lane quarter) and
 //               128 of the 256 columns; FP32 accumulators live in registers.
 // TMEM holds two 256-column FP32 partial buffers so the tensor core computes
-// slice k+1 while the epilogue promotes slice k.  Every wait is bounded; a
-// wait that runs out raises MOE_DEV_TIMEOUT in *device_status and the CTA
-// winds down (draining its copies and MMAs, freeing TMEM).
+// slice k+1 while the epilogue promotes slice k.  A stage is refilled only
+// after the MMA has consumed it and every epilogue warp has read its scales.
+// The epilogue issues no global loads: under the weight stream a plain load
+// waits behind the TMA traffic for several microseconds.
+// Every wait is bounded; a wait that runs out raises MOE_DEV_TIMEOUT in
+// *device_status and the CTA winds down (draining its copies and MMAs,
+// freeing TMEM).
 #include <mutex>
 
 #include "common.cuh"
@@ -41,11 +49,22 @@ constexpr int kTileN = 256;
 constexpr int kTileK = 128;
 constexpr int kABytes = kTileM * kTileK;  // 16 KiB
 constexpr int kBBytes = kTileN * kTileK;  // 32 KiB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kNumEpiWarps = 8;
 constexpr int kNumThreads = 64 + 32 * kNumEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, kTileN);
+constexpr int kMaxBlocksSmem = 2048;  // plan blocks whose expert id is cached in shared memory
+constexpr int kRowPad = kTileM;       // staged per-slot arrays carry this many extra slots
+
+// Per-stage side data, filled by bulk copies next to the operand tiles.
+struct StageExtra {
+  float a_scale[kTileM];     // activation (up) / intermediate (down) scale of each tile row
+  float4 w_scale;            // the tile's two weight block scales for this K slice
+  uint8_t pad0[496];
+  int32_t tok[kTileM];       // down, first slice of a tile: token of each row (-1 = no route)
+  float weight[kTileM];      // down, first slice of a tile: route weight x routed scale
+};
+static_assert(sizeof(StageExtra) == 2048, "stage extra layout");
 
 struct SmemCtl {
   uint64_t full[kStages];
@@ -55,36 +74,41 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int pad[2];
-  float xchg[2][2][kTileM];  // [tile parity][column half][row]: amax exchange
+  float xchg[2][2][kTileM];        // [tile parity][column half][row]: amax exchange
+  int32_t expert[kMaxBlocksSmem];  // expert of each plan block (cached at start)
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemCtl);
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + sizeof(StageExtra)) + sizeof(SmemCtl);
 
 struct GemmParams {
-  const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* num_post_padded;
-  const float* a_scale;   // up: [M, nkb] per token; down: [sorted_cap, nkb] per plan slot
-  const float* b_scale;   // up: w13_scale [E, 2I/128, nkb]; down: w2_scale [E, H/128, nkb]
-  const float* topk_w;    // down: [M * top_k]
-  float* acc_out;         // down: [M, H]
-  uint8_t* q_inter;       // up: [sorted_cap, I]
-  float* s_inter;         // up: [sorted_cap, I/128]
-  uint8_t* dbg_q;         // up, nullable
-  float* dbg_s;           // up, nullable
-  int32_t* status;        // nullable
-  int64_t nblocks;        // plan block slots the grid walks
+  const int32_t* sorted_ids;   // up with gather4: plan (token of each row)
+  const float* a_scale_t;      // [nkb, cap_pad]: scale of each plan slot per K slice
+  const float4* w_scale_st;    // [nblocks, ntiles_n, nkb]: weight scales per tile and slice
+  const int32_t* slot_tok;     // down: [cap_pad] token per plan slot (-1 = pad)
+  const float* slot_w;         // down: [cap_pad] route weight x routed scale
+  float* acc_out;              // down: [M, H]
+  uint8_t* q_inter;            // up: [sorted_cap, I]
+  float* s_inter_t;            // up: [I/128, cap_pad]
+  uint8_t* dbg_q;              // up, nullable: [sorted_cap, I]
+  float* dbg_s;                // up, nullable: [sorted_cap, I/128]
+  int32_t* status;             // nullable
+  int64_t nblocks;             // plan block slots the grid walks
+  int64_t cap_pad;             // row stride of the staged per-slot arrays
   int R;
   int top_k;
   int block_m;
   int E;
-  int nkb;                // K / 128
-  int ntiles_n;           // 256-wide output tiles per expert
-  int b_rows;             // weight rows per expert (2I or H)
-  int b_row_blocks;       // b_rows / 128 rounded up
+  int nkb;                     // K / 128
+  int ntiles_n;                // 256-wide output tiles per expert
+  int b_rows;                  // weight rows per expert (2I or H)
   int I;
   int H;
-  float routed_scale;
+  int a_gather4;               // up only: 1 = activation rows fetched by token with tile::gather4,
+                               //          0 = rows already in plan order (2D boxes by plan slot)
+  int block_major;             // tile order: 1 = all n tiles of a plan block together, 0 = n-tile major
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -103,16 +127,37 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+__device__ __forceinline__ int block_expert(const GemmParams& p, const SmemCtl* ctl, int64_t b) {
+  return b < kMaxBlocksSmem ? ctl->expert[b] : p.expert_ids[b];
+}
+
 // Tile -> (plan block, n tile, expert); false if the tile has no work.
-__device__ __forceinline__ bool tile_coords(const GemmParams& p, int64_t tile, int64_t nvalid, int& b, int& t, int& e) {
-  b = static_cast<int>(tile % p.nblocks);
-  t = static_cast<int>(tile / p.nblocks);
+__device__ __forceinline__ bool tile_coords(const GemmParams& p, const SmemCtl* ctl, int64_t tile, int64_t nvalid,
+                                            int& b, int& t, int& e) {
+  if (p.block_major) {
+    b = static_cast<int>(tile / p.ntiles_n);
+    t = static_cast<int>(tile % p.ntiles_n);
+  } else {
+    b = static_cast<int>(tile % p.nblocks);
+    t = static_cast<int>(tile / p.nblocks);
+  }
   if (b >= nvalid) return false;
-  e = p.expert_ids[b];
+  e = block_expert(p, ctl, b);
   return e >= 0 && e < p.E;
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+// silu(g) = g / (1 + exp(-g)) with the hardware exp2 and divide
+// approximations (a few ulp; for g below about -88 the quotient is 0).
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Plan entries of the four rows 4*lane .. 4*lane+3 of plan block b (gather4 path).
+__device__ __forceinline__ void load_ids(const GemmParams& p, int b, int lane, int (&id)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * lane + i;
+    id[i] = r < p.block_m ? p.sorted_ids[static_cast<int64_t>(b) * p.block_m + r] : -1;
+  }
+}
 
 template <bool kUp>
 __global__ void __launch_bounds__(kNumThreads, 1)
@@ -122,7 +167,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  StageExtra* sX = reinterpret_cast<StageExtra*>(sB + kStages * kBBytes);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sX + kStages);
   volatile int* abort_flag = &ctl->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -131,7 +177,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1 + kNumEpiWarps);  // MMA commit + every epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -146,35 +192,49 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = ctl->tmem_base;
-
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
   if (nvalid > p.nblocks) nvalid = p.nblocks;
+  const int64_t ncache = nvalid < kMaxBlocksSmem ? nvalid : kMaxBlocksSmem;
+  for (int64_t b = threadIdx.x; b < ncache; b += blockDim.x) ctl->expert[b] = p.expert_ids[b];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
   const int64_t total = p.nblocks * p.ntiles_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      int b, t, e;
-      if (!tile_coords(p, tile, nvalid, b, t, e)) continue;
+    int64_t tile = blockIdx.x;
+    int b = 0, t = 0, e = 0;
+    while (tile < total && !tile_coords(p, ctl, tile, nvalid, b, t, e)) tile += gridDim.x;
+    // gather4 path: a tile's plan entries are read one tile ahead
+    int ids[4] = {-1, -1, -1, -1};
+    if (kUp && p.a_gather4 && tile < total) load_ids(p, b, lane, ids);
+    while (tile < total && ok) {
+      int64_t ntile = tile + gridDim.x;
+      int nb = 0, nt = 0, ne = 0;
+      while (ntile < total && !tile_coords(p, ctl, ntile, nvalid, nb, nt, ne)) ntile += gridDim.x;
       int tok[4] = {0, 0, 0, 0};
-      if (kUp) {
+      bool mine = false;                 // this lane's four rows hold a route
+      uint32_t a_bytes = kABytes;
+      if (kUp && p.a_gather4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = 4 * lane + i;
-          int id = -1;
-          if (r < p.block_m) id = p.sorted_ids[static_cast<int64_t>(b) * p.block_m + r];
-          tok[i] = (id >= 0 && id < p.R) ? id / p.top_k : 0;
+          const bool route = ids[i] >= 0 && ids[i] < p.R;
+          mine |= route;
+          tok[i] = route ? ids[i] / p.top_k : 0;
         }
+        // only groups with a route are fetched; the other rows keep stale
+        // shared memory, whose products land in rows the epilogue ignores
+        a_bytes = 512u * static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, mine)));
+        if (ntile < total) load_ids(p, nb, lane, ids);
       }
       const int brow = e * p.b_rows + t * kTileN;
+      const int64_t slot0 = static_cast<int64_t>(b) * p.block_m;
       for (int kb = 0; kb < p.nkb; ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
@@ -183,17 +243,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           break;
         }
         const uint32_t full = smem_u32(&ctl->full[s]);
-        if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+        const bool tile_info = !kUp && kb == 0;
+        const uint32_t extra = 512u + 16u + (tile_info ? 1024u : 0u);
+        if (lane == 0) mbar_arrive_expect_tx(full, a_bytes + kBBytes + extra);
         __syncwarp();
         const uint32_t a_dst = smem_u32(sA + s * kABytes);
-        if (kUp) {
-          tma_gather4(a_dst + 512u * lane, &tmA, full, kb * kTileK, tok[0], tok[1], tok[2], tok[3]);
+        if (kUp && p.a_gather4) {
+          if (mine) tma_gather4(a_dst + 512u * lane, &tmA, full, kb * kTileK, tok[0], tok[1], tok[2], tok[3]);
         } else if (lane == 0) {
           tma_load_2d(a_dst, &tmA, full, kb * kTileK, b * p.block_m);
         }
-        if (lane == 0) tma_load_2d(smem_u32(sB + s * kBBytes), &tmB, full, kb * kTileK, brow);
+        if (lane == 0) {
+          tma_load_2d(smem_u32(sB + s * kBBytes), &tmB, full, kb * kTileK, brow);
+          StageExtra* x = sX + s;
+          bulk_load(smem_u32(x->a_scale), p.a_scale_t + kb * p.cap_pad + slot0, 512u, full);
+          bulk_load(smem_u32(&x->w_scale), p.w_scale_st + (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb, 16u,
+                    full);
+          if (tile_info) {
+            bulk_load(smem_u32(x->tok), p.slot_tok + slot0, 512u, full);
+            bulk_load(smem_u32(x->weight), p.slot_w + slot0, 512u, full);
+          }
+        }
         ++it;
       }
+      tile = ntile;
+      b = nb;
+      t = nt;
+      e = ne;
     }
     if (!ok && lane == 0) {
       // wind down: let the copies already issued land before the CTA exits
@@ -207,7 +283,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         int b, t, e;
-        if (!tile_coords(p, tile, nvalid, b, t, e)) continue;
+        if (!tile_coords(p, ctl, tile, nvalid, b, t, e)) continue;
         for (int kb = 0; kb < p.nkb; ++kb) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -239,63 +315,65 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
+    const bool rvalid = row < p.block_m;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
     int tcount = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int b, t, e;
-      if (!tile_coords(p, tile, nvalid, b, t, e)) {
+      if (!tile_coords(p, ctl, tile, nvalid, b, t, e)) {
         if (warp == 2 && lane == 0 && t == 0 && static_cast<int64_t>(b) < nvalid) {
-          const int bad = p.expert_ids[b];
+          const int bad = block_expert(p, ctl, b);
           if (bad != -1) report(p.status, MOE_DEV_BAD_EXPERT);
         }
         continue;
       }
       const int64_t slot = static_cast<int64_t>(b) * p.block_m + row;
-      const bool rvalid = row < p.block_m;
-      const int id = rvalid ? p.sorted_ids[slot] : -1;
-      const bool is_route = id >= 0 && id < p.R;
-
-      const float* as_row;
-      const float* ws0;
-      const float* ws1;
-      bool cols_valid = true;
-      if (kUp) {
-        const int tok = is_route ? id / p.top_k : 0;
-        as_row = p.a_scale + static_cast<int64_t>(tok) * p.nkb;
-        ws0 = p.b_scale + (static_cast<int64_t>(e) * p.b_row_blocks + t) * p.nkb;                  // gate block
-        ws1 = p.b_scale + (static_cast<int64_t>(e) * p.b_row_blocks + p.I / 128 + t) * p.nkb;      // up block
-      } else {
-        const int hblk = 2 * t + half;
-        cols_valid = hblk < p.b_row_blocks;
-        as_row = p.a_scale + (rvalid ? slot : 0) * p.nkb;
-        ws0 = p.b_scale + (static_cast<int64_t>(e) * p.b_row_blocks + (cols_valid ? hblk : 0)) * p.nkb;
-        ws1 = ws0;
-      }
+      int tok = -1;
+      float wr = 0.f;
 
       float acc[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) acc[c] = 0.f;
 
       for (int kb = 0; kb < p.nkb; ++kb) {
-        const float as = rvalid ? __ldg(as_row + kb) : 0.f;
-        const float s0 = __fmul_rn(as, __ldg(ws0 + kb));
-        const float s1 = kUp ? __fmul_rn(as, __ldg(ws1 + kb)) : s0;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
         const uint32_t tb = it & 1u;
         const uint32_t tph = (it >> 1) & 1u;
+        // the slice's scales (and the tile's row data) arrive with the stage
+        float s0 = 0.f, s1 = 0.f;
+        if (ok) ok = warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag);
+        if (ok) {
+          const StageExtra* x = sX + s;
+          const float as = x->a_scale[row];
+          const float4 ws = x->w_scale;
+          if (kUp) {
+            s0 = __fmul_rn(as, ws.x);  // gate block
+            s1 = __fmul_rn(as, ws.y);  // up block
+          } else {
+            s0 = __fmul_rn(as, half == 0 ? ws.x : ws.y);
+            if (kb == 0) {
+              tok = x->tok[row];
+              wr = x->weight[row];
+            }
+          }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
         if (ok) ok = warp_wait(smem_u32(&ctl->tfull[tb]), tph, abort_flag);
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(lane_base + tb * kTileN + 128u * half + 32u * ch, v);
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(lane_base + tb * kTileN + 128u * half + 16u * ch, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float sc = (kUp && (i & 8)) ? s1 : s0;
-              acc[32 * ch + i] = fmaf(__uint_as_float(v[i]), sc, acc[32 * ch + i]);
+            for (int i = 0; i < 16; ++i) {
+              const float sc = (kUp && (i & 8)) ? s1 : s0;  // up kernel: gate columns 0-7, up columns 8-15
+              acc[16 * ch + i] = fmaf(__uint_as_float(v[i]), sc, acc[16 * ch + i]);
             }
           }
           tc_fence_before();
@@ -322,24 +400,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         named_barrier(1, 32 * kNumEpiWarps);
         amax = fmaxf(amax, ctl->xchg[tcount & 1][half ^ 1][row]);
         const float s = __fdiv_rn(amax, 448.0f);
+        // h / s as h * (1/s): the two roundings can move a value across an
+        // E4M3 rounding midpoint only when it lies within an ulp of it
+        const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
         if (ok && rvalid) {
           uint32_t packed[16];
 #pragma unroll
           for (int w = 0; w < 16; ++w) {
-            uint32_t word = 0;
-            if (s > 0.f) {
-              const uint16_t lo = cvt_e4m3x2(__fdiv_rn(acc[4 * w + 0], s), __fdiv_rn(acc[4 * w + 1], s));
-              const uint16_t hi = cvt_e4m3x2(__fdiv_rn(acc[4 * w + 2], s), __fdiv_rn(acc[4 * w + 3], s));
-              word = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-            }
-            packed[w] = word;
+            const uint16_t lo = cvt_e4m3x2(__fmul_rn(acc[4 * w + 0], inv), __fmul_rn(acc[4 * w + 1], inv));
+            const uint16_t hi = cvt_e4m3x2(__fmul_rn(acc[4 * w + 2], inv), __fmul_rn(acc[4 * w + 3], inv));
+            packed[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
           }
           const int64_t qoff = slot * p.I + 128 * t + 64 * half;
           uint4* qdst = reinterpret_cast<uint4*>(p.q_inter + qoff);
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             qdst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
-          if (half == 0) p.s_inter[slot * (p.I / 128) + t] = s;
+          if (half == 0) p.s_inter_t[static_cast<int64_t>(t) * p.cap_pad + slot] = s;
           if (p.dbg_q) {
             uint4* ddst = reinterpret_cast<uint4*>(p.dbg_q + qoff);
 #pragma unroll
@@ -348,14 +425,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (half == 0) p.dbg_s[slot * (p.I / 128) + t] = s;
           }
         }
-      } else if (ok && is_route && cols_valid) {
-        const float wr = __fmul_rn(__ldg(p.topk_w + id), p.routed_scale);
-        const int tok = id / p.top_k;
-        float* dst = p.acc_out + static_cast<int64_t>(tok) * p.H + (2 * t + half) * 128;
+      } else {
+        const int hblk = 2 * t + half;
+        if (ok && rvalid && tok >= 0 && hblk < p.H / 128) {
+          float* dst = p.acc_out + static_cast<int64_t>(tok) * p.H + hblk * 128;
 #pragma unroll
-        for (int c = 0; c < 128; c += 4)
-          red_add_v4(dst + c, __fmul_rn(acc[c], wr), __fmul_rn(acc[c + 1], wr), __fmul_rn(acc[c + 2], wr),
-                     __fmul_rn(acc[c + 3], wr));
+          for (int c = 0; c < 128; c += 4)
+            red_add_v4(dst + c, __fmul_rn(acc[c], wr), __fmul_rn(acc[c + 1], wr), __fmul_rn(acc[c + 2], wr),
+                       __fmul_rn(acc[c + 3], wr));
+        }
       }
       ++tcount;
     }
@@ -366,6 +444,94 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_after();
   if (threadIdx.x == 0 && ctl->abort_flag) report(p.status, MOE_DEV_TIMEOUT);
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Staging for the GEMM kernels (launch 0).  Part 1, one warp per plan slot
+// below P: token and route weight of the slot (-1 / 0 for pads), the
+// activation scales transposed to [nkb, cap_pad], and for well-filled plans
+// the activation row copied into plan order.  Part 2, per plan block below P
+// with a valid expert: the 16-byte weight-scale records of every (n tile,
+// K slice) of both GEMMs.
+struct StageParams {
+  const uint8_t* a;
+  const float* a_scale;
+  const float* topk_w;
+  const int32_t* sorted_ids;
+  const int32_t* expert_ids;
+  const int32_t* num_post_padded;
+  const float* w13_scale;
+  const float* w2_scale;
+  uint8_t* a_sorted;          // nullable: no row copy
+  float* as_t;                // [nkb, cap_pad]
+  int32_t* slot_tok;          // [cap_pad]
+  float* slot_w;              // [cap_pad]
+  float4* wsu;                // [nblocks, I/128, H/128]
+  float4* wsd;                // [nblocks, ceil(H/256), I/128]
+  int64_t nblocks;
+  int64_t cap_pad;
+  int R, top_k, block_m, E, H, I;
+  float routed_scale;
+};
+
+__global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
+  int64_t P = *p.num_post_padded;
+  if (P < 0) P = 0;
+  int64_t nvalid = P / p.block_m;
+  if (nvalid > p.nblocks) nvalid = p.nblocks;
+  const int64_t nslots = nvalid * p.block_m;
+  const int lane = threadIdx.x % 32;
+  const int64_t gtid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  const int nkb = p.H / 128, nib = p.I / 128;
+  const int chunks = p.H / 16;
+  for (int64_t slot = gtid / 32; slot < nslots; slot += nwarps) {
+    const int id = p.sorted_ids[slot];
+    const bool route = id >= 0 && id < p.R;
+    const int64_t tok = route ? id / p.top_k : 0;
+    if (lane == 0) {
+      p.slot_tok[slot] = route ? static_cast<int32_t>(tok) : -1;
+      p.slot_w[slot] = route ? __fmul_rn(__ldg(p.topk_w + id), p.routed_scale) : 0.f;
+    }
+    if (!route) continue;
+    for (int k = lane; k < nkb; k += 32) p.as_t[k * p.cap_pad + slot] = __ldg(p.a_scale + tok * nkb + k);
+    if (p.a_sorted) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.a + tok * p.H);
+      uint4* dst = reinterpret_cast<uint4*>(p.a_sorted + slot * p.H);
+      int c = lane;
+      for (; c + 96 < chunks; c += 128) {
+        const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64), v3 = __ldg(src + c + 96);
+        dst[c] = v0;
+        dst[c + 32] = v1;
+        dst[c + 64] = v2;
+        dst[c + 96] = v3;
+      }
+      for (; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    }
+  }
+  // weight-scale records
+  const int up_items = nib * nkb;          // (n tile: I/128 of them) x (K slice)
+  const int nh = (p.H + 255) / 256;
+  const int dn_items = nh * nib;
+  const int per_block = up_items + dn_items;
+  const int nrb13 = 2 * p.I / 128, nrb2 = p.H / 128;
+  for (int64_t i = gtid; i < nvalid * per_block; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = i / per_block;
+    const int j = static_cast<int>(i - b * per_block);
+    const int e = p.expert_ids[b];
+    if (e < 0 || e >= p.E) continue;
+    if (j < up_items) {
+      const int t = j / nkb, kb = j % nkb;
+      const float* base = p.w13_scale + static_cast<int64_t>(e) * nrb13 * nkb;
+      p.wsu[b * up_items + j] = make_float4(base[t * nkb + kb], base[(nib + t) * nkb + kb], 0.f, 0.f);
+    } else {
+      const int jj = j - up_items;
+      const int h = jj / nib, ib = jj % nib;
+      const float* base = p.w2_scale + static_cast<int64_t>(e) * nrb2 * nib;
+      const float lo = base[(2 * h) * nib + ib];
+      const float hi = (2 * h + 1 < nrb2) ? base[(2 * h + 1) * nib + ib] : 0.f;
+      p.wsd[b * dn_items + jj] = make_float4(lo, hi, 0.f, 0.f);
+    }
+  }
 }
 
 // out = bf16_rn(f32(out) + acc); acc = 0.  Eight elements per thread.
@@ -392,16 +558,52 @@ __global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ ou
   }
 }
 
+// Activation rows are copied into plan order when plan blocks are well
+// filled (at least 8 routes per touched expert on average): tile::gather4
+// moves one 128-byte row per ~35 cycles per SM on GB300, far below the rate
+// of 2D boxes, and would fetch every row once per 256-wide N tile.  Sparse
+// (decode-sized) plans keep gather4 and fetch only groups holding a route.
+bool use_pregather(int64_t R, int E) {
+  const int64_t nonempty = R < E ? R : E;
+  return nonempty > 0 && R >= 8 * nonempty;
+}
+
+// Plan blocks that can hold work: P <= R + min(E, R) * (block_m - 1).
+int64_t block_bound(int64_t R, int E, int block_m) {
+  const int64_t nonempty = R < E ? R : E;
+  return ceil_div(R + nonempty * (block_m - 1), block_m);
+}
+
 struct WsLayout {
-  size_t acc_off, q_off, s_off, total;
+  size_t acc_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, total;
+  int64_t cap_pad, nblocks;
+  bool pregather;
 };
 
-WsLayout ws_layout(int64_t M, int H, int I, int64_t sorted_cap) {
+WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64_t sorted_cap) {
   WsLayout l;
-  l.acc_off = 0;
-  l.q_off = static_cast<size_t>(round_up(M * H * 4, 256));
-  l.s_off = l.q_off + static_cast<size_t>(round_up(sorted_cap * I, 256));
-  l.total = l.s_off + static_cast<size_t>(round_up(sorted_cap * (I / 128) * 4, 256));
+  const int64_t R = M * top_k;
+  l.pregather = use_pregather(R, E);
+  l.cap_pad = round_up(sorted_cap + kRowPad, 8);  // keeps every 512-byte slice 16-byte aligned
+  l.nblocks = block_bound(R, E, block_m);
+  if (l.nblocks > sorted_cap / block_m) l.nblocks = sorted_cap / block_m;
+  const int nkb = H / 128, nib = I / 128, nh = (H + 255) / 256;
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const size_t at = off;
+    off += static_cast<size_t>(round_up(bytes, 256));
+    return at;
+  };
+  l.acc_off = take(M * H * 4);
+  l.q_off = take(sorted_cap * I);
+  l.st_off = take(static_cast<int64_t>(nib) * l.cap_pad * 4);
+  l.ast_off = take(static_cast<int64_t>(nkb) * l.cap_pad * 4);
+  l.tok_off = take(l.cap_pad * 4);
+  l.w_off = take(l.cap_pad * 4);
+  l.wsu_off = take(l.nblocks * nib * nkb * 16);
+  l.wsd_off = take(l.nblocks * nh * nib * 16);
+  l.a_off = take(l.pregather ? sorted_cap * H : 0);
+  l.total = off;
   return l;
 }
 
@@ -425,11 +627,9 @@ bool set_smem_attrs(int device) {
 
 extern "C" {
 
-size_t moe_forward_workspace_size(int64_t M, int H, int I, int top_k, int block_m, int64_t sorted_cap) {
-  (void)top_k;
-  (void)block_m;
-  if (M < 0 || H < 0 || I < 0 || sorted_cap < 0) return 0;
-  return moe::ws_layout(M, H, I, sorted_cap).total;
+size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int block_m, int64_t sorted_cap) {
+  if (M < 0 || H < 0 || I < 0 || E < 1 || top_k < 1 || block_m < 1 || sorted_cap < 0) return 0;
+  return moe::ws_layout(M, H, I, E, top_k, block_m, sorted_cap).total;
 }
 
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t stream) {
@@ -441,7 +641,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   if (a->blocks_cap < 1 || a->sorted_cap < a->blocks_cap * a->block_m) return MOE_ERR_CAPACITY;
   const int64_t R = a->M * a->top_k;
   if (R >= (int64_t(1) << 31) - 1 || static_cast<int64_t>(a->E) * 2 * a->I >= (int64_t(1) << 31) ||
-      static_cast<int64_t>(a->E) * a->H >= (int64_t(1) << 31) || a->sorted_cap >= (int64_t(1) << 31))
+      static_cast<int64_t>(a->E) * a->H >= (int64_t(1) << 31) || a->sorted_cap >= (int64_t(1) << 30))
     return MOE_ERR_SHAPE;
   if (a->M == 0) return MOE_OK;
   if (!a->a || !a->a_scale || !a->w13 || !a->w13_scale || !a->w2 || !a->w2_scale || !a->topk_weights ||
@@ -451,7 +651,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   if (!aligned16(a->a) || !aligned16(a->w13) || !aligned16(a->w2) || !aligned16(a->workspace) ||
       !aligned16(a->out) || (a->debug_q_inter && !aligned16(a->debug_q_inter)))
     return MOE_ERR_ALIGN;
-  const WsLayout wl = ws_layout(a->M, a->H, a->I, a->sorted_cap);
+  const WsLayout wl = ws_layout(a->M, a->H, a->I, a->E, a->top_k, a->block_m, a->sorted_cap);
   if (a->workspace_bytes < wl.total) return MOE_ERR_CAPACITY;
 
   DeviceInfo dev;
@@ -469,11 +669,21 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   float* acc = reinterpret_cast<float*>(ws + wl.acc_off);
   uint8_t* q_inter = ws + wl.q_off;
-  float* s_inter = reinterpret_cast<float*>(ws + wl.s_off);
+  float* s_inter_t = reinterpret_cast<float*>(ws + wl.st_off);
+  float* as_t = reinterpret_cast<float*>(ws + wl.ast_off);
+  int32_t* slot_tok = reinterpret_cast<int32_t*>(ws + wl.tok_off);
+  float* slot_w = reinterpret_cast<float*>(ws + wl.w_off);
+  float4* wsu = reinterpret_cast<float4*>(ws + wl.wsu_off);
+  float4* wsd = reinterpret_cast<float4*>(ws + wl.wsd_off);
+  uint8_t* a_sorted = wl.pregather ? ws + wl.a_off : nullptr;
 
   const int N = 2 * a->I;
   CUtensorMap tm_a, tm_w13, tm_q, tm_w2;
-  if (encode_tensor_map_2d(&tm_a, a->a, a->H, a->M, a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+  const CUresult ra = wl.pregather
+                          ? encode_tensor_map_2d(&tm_a, a_sorted, a->H, a->sorted_cap, a->H, 128, 128,
+                                                 CU_TENSOR_MAP_SWIZZLE_128B)
+                          : encode_tensor_map_2d(&tm_a, a->a, a->H, a->M, a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ra != CUDA_SUCCESS ||
       encode_tensor_map_2d(&tm_w13, a->w13, a->H, static_cast<uint64_t>(a->E) * N, a->H, 128, 256,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tensor_map_2d(&tm_q, q_inter, a->I, a->sorted_cap, a->I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
@@ -482,39 +692,67 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
 
-  // Plan blocks that can hold work: P <= R + min(E, R) * (block_m - 1).
-  const int64_t nonempty = R < a->E ? R : a->E;
-  int64_t nblocks = ceil_div(R + nonempty * (a->block_m - 1), a->block_m);
+  int64_t nblocks = wl.nblocks;
   if (nblocks > a->blocks_cap) nblocks = a->blocks_cap;
-
-  GemmParams p{};
-  p.sorted_ids = a->sorted_token_ids;
-  p.expert_ids = a->expert_ids;
-  p.num_post_padded = a->num_tokens_post_padded;
-  p.status = a->device_status;
-  p.nblocks = nblocks;
-  p.R = static_cast<int>(R);
-  p.top_k = a->top_k;
-  p.block_m = a->block_m;
-  p.E = a->E;
-  p.I = a->I;
-  p.H = a->H;
-  p.routed_scale = a->routed_scale;
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
   if (nblocks > 0) {
+    StageParams sp{};
+    sp.a = a->a;
+    sp.a_scale = a->a_scale;
+    sp.topk_w = a->topk_weights;
+    sp.sorted_ids = a->sorted_token_ids;
+    sp.expert_ids = a->expert_ids;
+    sp.num_post_padded = a->num_tokens_post_padded;
+    sp.w13_scale = a->w13_scale;
+    sp.w2_scale = a->w2_scale;
+    sp.a_sorted = a_sorted;
+    sp.as_t = as_t;
+    sp.slot_tok = slot_tok;
+    sp.slot_w = slot_w;
+    sp.wsu = wsu;
+    sp.wsd = wsd;
+    sp.nblocks = nblocks;
+    sp.cap_pad = wl.cap_pad;
+    sp.R = static_cast<int>(R);
+    sp.top_k = a->top_k;
+    sp.block_m = a->block_m;
+    sp.E = a->E;
+    sp.H = a->H;
+    sp.I = a->I;
+    sp.routed_scale = a->routed_scale;
+    int64_t sgrid = ceil_div(nblocks * a->block_m, 8);
+    if (sgrid > static_cast<int64_t>(dev.sms) * 8) sgrid = static_cast<int64_t>(dev.sms) * 8;
+    stage_kernel<<<static_cast<unsigned>(sgrid), 256, 0, stream>>>(sp);
+    MOE_CUDA_TRY(cudaGetLastError());
+
+    GemmParams p{};
+    p.expert_ids = a->expert_ids;
+    p.num_post_padded = a->num_tokens_post_padded;
+    p.sorted_ids = a->sorted_token_ids;
+    p.status = a->device_status;
+    p.nblocks = nblocks;
+    p.cap_pad = wl.cap_pad;
+    p.R = static_cast<int>(R);
+    p.top_k = a->top_k;
+    p.block_m = a->block_m;
+    p.E = a->E;
+    p.I = a->I;
+    p.H = a->H;
+
     GemmParams up = p;
-    up.a_scale = a->a_scale;
-    up.b_scale = a->w13_scale;
+    up.a_scale_t = as_t;
+    up.w_scale_st = wsu;
     up.q_inter = q_inter;
-    up.s_inter = s_inter;
+    up.s_inter_t = s_inter_t;
     up.dbg_q = a->debug_q_inter;
     up.dbg_s = a->debug_s_inter;
     up.nkb = a->H / 128;
     up.ntiles_n = N / kTileN;
     up.b_rows = N;
-    up.b_row_blocks = N / 128;
+    up.a_gather4 = wl.pregather ? 0 : 1;
+    up.block_major = 1;
     const int64_t up_tiles = nblocks * up.ntiles_n;
     const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
     moe_gemm_kernel<true><<<up_grid, kNumThreads, kSmemBytes, stream>>>(tm_a, tm_w13, up);
@@ -522,14 +760,16 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
 
     GemmParams dn = p;
-    dn.a_scale = s_inter;
-    dn.b_scale = a->w2_scale;
-    dn.topk_w = a->topk_weights;
+    dn.a_scale_t = s_inter_t;
+    dn.w_scale_st = wsd;
+    dn.slot_tok = slot_tok;
+    dn.slot_w = slot_w;
     dn.acc_out = acc;
     dn.nkb = a->I / 128;
     dn.ntiles_n = static_cast<int>(ceil_div(a->H, kTileN));
     dn.b_rows = a->H;
-    dn.b_row_blocks = a->H / 128;
+    dn.a_gather4 = 0;
+    dn.block_major = 0;
     const int64_t dn_tiles = nblocks * dn.ntiles_n;
     const int dn_grid = static_cast<int>(dn_tiles < dev.sms ? dn_tiles : dev.sms);
     moe_gemm_kernel<false><<<dn_grid, kNumThreads, kSmemBytes, stream>>>(tm_q, tm_w2, dn);

@@ -43,8 +43,9 @@ moe_status moe_fp8_block_scale_forward_noalloc(const moe_fwd_args* args, moe_str
   using namespace moe;
   if (!args) return MOE_ERR_NULL;
   if (args->M < 0 || args->H < 0 || args->I < 0 || args->sorted_cap < 0) return MOE_ERR_SHAPE;
-  const size_t need = moe_forward_workspace_size(args->M, args->H, args->I, args->top_k, args->block_m,
+  const size_t need = moe_forward_workspace_size(args->M, args->H, args->I, args->E, args->top_k, args->block_m,
                                                  args->sorted_cap);
+  if (need == 0) return MOE_ERR_SHAPE;
   if (need > kStaticScratchBytes) return MOE_ERR_CAPACITY;
   if (args->M == 0) return MOE_OK;
   DeviceInfo dev;

@@ -8,9 +8,9 @@
 //               stable rank among same-expert routes of its chunk (warp
 //               match + per-warp histograms in shared memory) and the chunk's
 //               per-expert counts.
-//   2. scan:    one CTA turns the [chunks x E] counts into per-chunk bases,
-//               pads each expert to block_m, scans the experts, writes
-//               expert_ids, the pad sentinels and P.
+//   2. scan:    one CTA: a warp per expert scans that expert's per-chunk
+//               counts into bases, then the experts' padded lengths are
+//               scanned; writes expert_ids, the pad sentinels and P.
 //   3. scatter: sorted_token_ids[base(chunk, e) + rank] = r.
 // No inter-CTA waits; the same ids always give the same bytes.
 #include "common.cuh"
@@ -24,9 +24,10 @@ constexpr int kScanThreads = 1024;
 constexpr int kMaxExperts = 2048;
 
 struct PlanWs {
-  int32_t* counts;  // [chunks, E]: chunk counts, then absolute bases
+  int32_t* counts;  // [E, chunks]: per-chunk counts, then bases inside the expert
   int32_t* rank;    // [R] stable rank of each route inside its chunk (or -1)
   int32_t* seg;     // [E] segment start of each expert
+  int nchunks;
 };
 
 __device__ __forceinline__ int load_id(const void* ids, int id_bits, int64_t r, int E) {
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(kChunk) plan_rank_kernel(const void* ids, int 
       wh[w * E + x] = run;
       run += v;
     }
-    ws.counts[static_cast<int64_t>(blockIdx.x) * E + x] = run;
+    ws.counts[static_cast<int64_t>(x) * ws.nchunks + blockIdx.x] = run;
   }
   __syncthreads();
   if (r < R) ws.rank[r] = e >= 0 ? wh[warp * E + e] + in_warp : -1;
@@ -94,27 +95,42 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
                                                                   int32_t* sorted_ids, int32_t* expert_ids,
                                                                   int32_t* num_post_padded) {
   __shared__ int scan_smem[33];
+  __shared__ int totals[kMaxExperts];
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  // 1. one warp per expert: exclusive scan of its chunk counts (bases inside
+  //    the expert) and the expert's total
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    int32_t* row = ws.counts + static_cast<int64_t>(e) * nchunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? row[c] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+      }
+      if (c < nchunks) row[c] = carry + inc - v;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) totals[e] = carry;
+  }
+  __syncthreads();
+  // 2. pad every expert to block_m and scan the experts
   constexpr int kPer = kMaxExperts / kScanThreads;  // experts per thread (2)
   int total[kPer], padded[kPer];
   int mine = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = threadIdx.x * kPer + i;
-    int run = 0;
-    if (e < E) {
-      for (int c = 0; c < nchunks; ++c) {
-        int32_t* p = ws.counts + static_cast<int64_t>(c) * E + e;
-        const int v = *p;
-        *p = run;  // exclusive base inside the expert
-        run += v;
-      }
-    }
-    total[i] = run;
-    padded[i] = (run + block_m - 1) / block_m * block_m;
+    total[i] = e < E ? totals[e] : 0;
+    padded[i] = (total[i] + block_m - 1) / block_m * block_m;
     mine += padded[i];
   }
   int P = 0;
   int start = block_exclusive_scan(mine, &P, scan_smem);
+  // 3. segment starts, pad sentinels, block experts, P
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = threadIdx.x * kPer + i;
@@ -135,7 +151,7 @@ __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, i
   const int rk = ws.rank[r];
   if (rk < 0) return;
   const int e = load_id(ids, id_bits, r, E);
-  const int base = ws.seg[e] + ws.counts[static_cast<int64_t>(blockIdx.x) * E + e];
+  const int base = ws.seg[e] + ws.counts[static_cast<int64_t>(e) * ws.nchunks + blockIdx.x];
   sorted_ids[base + rk] = static_cast<int32_t>(r);
 }
 
@@ -185,6 +201,7 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
   ws.rank = reinterpret_cast<int32_t*>(w);
   w += round_up(R * 4, 256);
   ws.seg = reinterpret_cast<int32_t*>(w);
+  ws.nchunks = static_cast<int>(R > 0 ? nchunks : 0);
 
   const size_t smem = static_cast<size_t>(kChunkWarps) * E * sizeof(int32_t);
   static bool attr_set[64] = {};

@@ -89,7 +89,7 @@ class DeviceProblem:
             self.expert_ids = torch.empty(bcap, dtype=torch.int32, device=dev)
         self.ntpp = torch.zeros(1, dtype=torch.int32, device=dev)
         self.plan_ws = torch.empty(max(L.moe_plan_workspace_size(M, k, E), 256), dtype=torch.uint8, device=dev)
-        ws_bytes = L.moe_forward_workspace_size(M, H, I, k, bm, cap)
+        ws_bytes = L.moe_forward_workspace_size(M, H, I, E, k, bm, cap)
         self.workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
         L.moe_workspace_init(self.workspace)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -185,10 +185,13 @@ typedef struct moe_fwd_args {
                                               kernel (per-kernel timing; no effect if NULL)  */
 } moe_fwd_args;
 
-/* Workspace bytes the forward needs (host-only).  The workspace holds the
- * requantised intermediate (sorted_cap x I codes and sorted_cap x I/128
- * scales) and an FP32 [M, H] route accumulator. */
-size_t moe_forward_workspace_size(int64_t M, int H, int I, int top_k, int block_m,
+/* Workspace bytes the forward needs (host-only; 0 for invalid sizes).  The
+ * workspace holds an FP32 [M, H] route accumulator, the requantised
+ * intermediate (sorted_cap x I codes and sorted_cap x I/128 scales) and, for
+ * well-filled plans (M * top_k >= 8 * min(E, M * top_k)), the activation rows
+ * and scales copied into plan order (sorted_cap x H bytes and
+ * sorted_cap x H/128 scales). */
+size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int block_m,
                                   int64_t sorted_cap);
 
 /* Zero a forward workspace (async).  A workspace must be zeroed once before

@@ -56,6 +56,6 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     args = L.MoeFwdArgs()
     args.M, args.H, args.I, args.E, args.top_k, args.block_m = 8192, 4096, 1024, 288, 8, 128
     args.sorted_cap, args.blocks_cap = 102400, 800
-    assert lib.moe_forward_workspace_size(8192, 4096, 1024, 8, 128, 102400) > cap_bytes
+    assert lib.moe_forward_workspace_size(8192, 4096, 1024, 288, 8, 128, 102400) > cap_bytes
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     assert lib.moe_fp8_block_scale_forward_noalloc(ctypes.byref(args), stream) == 4   # MOE_ERR_CAPACITY
