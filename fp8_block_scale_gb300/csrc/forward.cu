@@ -53,18 +53,23 @@ constexpr int kNumEpiWarps = 8;
 constexpr int kNumThreads = 64 + 32 * kNumEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, kTileN);
-constexpr int kMaxBlocksSmem = 2048;  // plan blocks whose expert id is cached in shared memory
+constexpr int kMaxBlocksSmem = 1024;  // plan blocks whose expert id is cached in shared memory
 constexpr int kRowPad = kTileM;       // staged per-slot arrays carry this many extra slots
 
 // Per-stage side data, filled by bulk copies next to the operand tiles.
 struct StageExtra {
   float a_scale[kTileM];     // activation (up) / intermediate (down) scale of each tile row
-  float4 w_scale;            // the tile's two weight block scales for this K slice
-  uint8_t pad0[496];
   int32_t tok[kTileM];       // down, first slice of a tile: token of each row (-1 = no route)
   float weight[kTileM];      // down, first slice of a tile: route weight x routed scale
+  float4 w_scale;            // the tile's two weight block scales for this K slice
+  float4 pad0;
 };
-static_assert(sizeof(StageExtra) == 2048, "stage extra layout");
+static_assert(sizeof(StageExtra) == 1568 && sizeof(StageExtra) % 16 == 0, "stage extra layout");
+
+// Down kernel: each epilogue warp transposes its 32 rows x 16 columns
+// through this buffer so that one vector reduction covers 8 rows x 64
+// contiguous bytes instead of 32 scattered rows.
+constexpr int kRedCols = 16;
 
 struct SmemCtl {
   uint64_t full[kStages];
@@ -75,6 +80,7 @@ struct SmemCtl {
   int abort_flag;
   int pad[2];
   float xchg[2][2][kTileM];        // [tile parity][column half][row]: amax exchange
+  float red[kNumEpiWarps][32][kRedCols + 4];  // down: per-warp transpose buffer (padded rows)
   int32_t expert[kMaxBlocksSmem];  // expert of each plan block (cached at start)
 };
 
@@ -427,12 +433,38 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
       } else {
         const int hblk = 2 * t + half;
-        if (ok && rvalid && tok >= 0 && hblk < p.H / 128) {
-          float* dst = p.acc_out + static_cast<int64_t>(tok) * p.H + hblk * 128;
+        if (ok && hblk < p.H / 128) {
+          // rows of this warp: quarter*32 + r; lane l reduces row 8*i + l/4,
+          // columns 4*(l%4) .. +3 of each 16-column chunk
+          const bool live = rvalid && tok >= 0;
+          if (__any_sync(0xffffffffu, live)) {
+          float (*buf)[kRedCols + 4] = ctl->red[warp - 2];
+          const int sub = lane >> 2, c4 = 4 * (lane & 3);
+          int toks[4];
+          float* dst[4];
 #pragma unroll
-          for (int c = 0; c < 128; c += 4)
-            red_add_v4(dst + c, __fmul_rn(acc[c], wr), __fmul_rn(acc[c + 1], wr), __fmul_rn(acc[c + 2], wr),
-                       __fmul_rn(acc[c + 3], wr));
+          for (int i = 0; i < 4; ++i) {
+            toks[i] = __shfl_sync(0xffffffffu, live ? tok : -1, 8 * i + sub);
+            dst[i] = p.acc_out + static_cast<int64_t>(toks[i] < 0 ? 0 : toks[i]) * p.H + hblk * 128 + c4;
+          }
+#pragma unroll
+          for (int ch = 0; ch < 128 / kRedCols; ++ch) {
+#pragma unroll
+            for (int j = 0; j < kRedCols; j += 4)
+              *reinterpret_cast<float4*>(&buf[lane][j]) =
+                  make_float4(__fmul_rn(acc[ch * kRedCols + j], wr), __fmul_rn(acc[ch * kRedCols + j + 1], wr),
+                              __fmul_rn(acc[ch * kRedCols + j + 2], wr), __fmul_rn(acc[ch * kRedCols + j + 3], wr));
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (toks[i] >= 0) {
+                const float4 v = *reinterpret_cast<const float4*>(&buf[8 * i + sub][c4]);
+                red_add_v4(dst[i] + ch * kRedCols, v.x, v.y, v.z, v.w);
+              }
+            }
+            __syncwarp();
+          }
+          }
         }
       }
       ++tcount;
@@ -535,26 +567,44 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
 }
 
 // out = bf16_rn(f32(out) + acc); acc = 0.  Eight elements per thread.
-__global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ out, float* __restrict__ acc, int64_t n8) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    uint4 o = reinterpret_cast<uint4*>(out)[i];
-    float4* ap = reinterpret_cast<float4*>(acc) + 2 * i;
-    const float4 a0 = ap[0];
-    const float4 a1 = ap[1];
-    ap[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    ap[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+__device__ __forceinline__ uint4 add_bf16x8(uint4 o, float4 a0, float4 a1) {
+  const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo = __fadd_rn(__uint_as_float((ow[k] & 0xFFFFu) << 16), av[2 * k]);
-      const float hi = __fadd_rn(__uint_as_float(ow[k] & 0xFFFF0000u), av[2 * k + 1]);
-      const uint32_t blo = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-      const uint32_t bhi = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-      ow[k] = blo | (bhi << 16);
-    }
-    reinterpret_cast<uint4*>(out)[i] = o;
+  for (int k = 0; k < 4; ++k) {
+    const float lo = __fadd_rn(__uint_as_float((ow[k] & 0xFFFFu) << 16), av[2 * k]);
+    const float hi = __fadd_rn(__uint_as_float(ow[k] & 0xFFFF0000u), av[2 * k + 1]);
+    const uint32_t blo = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t bhi = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    ow[k] = blo | (bhi << 16);
+  }
+  return o;
+}
+
+// Two groups of eight per iteration, all loads issued before any store.
+__global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ out, float* __restrict__ acc, int64_t n8) {
+  uint4* o4 = reinterpret_cast<uint4*>(out);
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  for (; i + stride < n8; i += 2 * stride) {
+    const int64_t j = i + stride;
+    const uint4 o0 = o4[i], o1 = o4[j];
+    const float4 a0 = a4[2 * i], a1 = a4[2 * i + 1], b0 = a4[2 * j], b1 = a4[2 * j + 1];
+    a4[2 * i] = z;
+    a4[2 * i + 1] = z;
+    a4[2 * j] = z;
+    a4[2 * j + 1] = z;
+    o4[i] = add_bf16x8(o0, a0, a1);
+    o4[j] = add_bf16x8(o1, b0, b1);
+  }
+  if (i < n8) {
+    const uint4 o0 = o4[i];
+    const float4 a0 = a4[2 * i], a1 = a4[2 * i + 1];
+    a4[2 * i] = z;
+    a4[2 * i + 1] = z;
+    o4[i] = add_bf16x8(o0, a0, a1);
   }
 }
 
@@ -781,7 +831,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
 
   const int64_t n8 = a->M * a->H / 8;
   int64_t fgrid = ceil_div(n8, 256);
-  if (fgrid > static_cast<int64_t>(dev.sms) * 8) fgrid = static_cast<int64_t>(dev.sms) * 8;
+  if (fgrid > static_cast<int64_t>(dev.sms) * 16) fgrid = static_cast<int64_t>(dev.sms) * 16;
   finalize_kernel<<<static_cast<unsigned>(fgrid), 256, 0, stream>>>(a->out, acc, n8);
   MOE_CUDA_TRY(cudaGetLastError());
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
