@@ -58,7 +58,11 @@ class MoeFwdArgs(ctypes.Structure):
         ("block_m", ctypes.c_int32),
         ("routed_scale", ctypes.c_float),
         ("profile_events", ctypes.POINTER(ctypes.c_void_p)),
+        ("tile_mode", ctypes.c_int32),
     ]
+
+
+TILE_AUTO, TILE_SINGLE, TILE_PAIR = 0, 1, 2
 
 
 _lib = None

@@ -43,7 +43,6 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kTileK = 128;
@@ -52,14 +51,24 @@ constexpr int kBBytes = kTileN * kTileK;  // 32 KiB
 constexpr int kNumEpiWarps = 8;
 constexpr int kNumThreads = 64 + 32 * kNumEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, kTileN);
+constexpr int kMaxStages = 5;
 constexpr int kMaxBlocksSmem = 1024;  // plan blocks whose expert id is cached in shared memory
 constexpr int kRowPad = kTileM;       // staged per-slot arrays carry this many extra slots
+
+// Single CTA: 4 stages of 16 KiB activation rows + the 32 KiB weight tile.
+// CTA pair (cta_group::2, M = 256 over two plan blocks of one expert): each
+// CTA holds its own 128 rows and half (128 rows) of the weight tile, so a
+// stage is 32 KiB and 5 stages fit.
+template <bool kPair> struct Cfg {
+  static constexpr int kStages = kPair ? 5 : 4;
+  static constexpr int kBStage = kPair ? kBBytes / 2 : kBBytes;
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(kPair ? 2 * kTileM : kTileM, kTileN);
+};
 
 // Per-stage side data, filled by bulk copies next to the operand tiles.
 struct StageExtra {
   float a_scale[kTileM];     // activation (up) / intermediate (down) scale of each tile row
-  int32_t tok[kTileM];       // down, first slice of a tile: token of each row (-1 = no route)
+  int32_t tok[kTileM];       // first slice of a tile: token of each row (-1 = no route)
   float weight[kTileM];      // down, first slice of a tile: route weight x routed scale
   float4 w_scale;            // the tile's two weight block scales for this K slice
   float4 pad0;
@@ -67,25 +76,38 @@ struct StageExtra {
 static_assert(sizeof(StageExtra) == 1568 && sizeof(StageExtra) % 16 == 0, "stage extra layout");
 
 // Down kernel: each epilogue warp transposes its 32 rows x 16 columns
-// through this buffer so that one vector reduction covers 8 rows x 64
+// through a buffer so that one vector reduction covers 8 rows x 64
 // contiguous bytes instead of 32 scattered rows.
 constexpr int kRedCols = 16;
 
 struct SmemCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];       // operand tiles landed (the leader's counts both CTAs of a pair)
+  uint64_t xfull[kMaxStages];      // this CTA's stage extras landed
+  uint64_t empty[kMaxStages];      // stage free: MMA done + every local epilogue warp read its extras
   uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tempty[2];              // (leader) TMEM buffer released by every epilogue warp of the pair
   uint32_t tmem_base;
   int abort_flag;
-  int pad[2];
-  float xchg[2][2][kTileM];        // [tile parity][column half][row]: amax exchange
-  float red[kNumEpiWarps][32][kRedCols + 4];  // down: per-warp transpose buffer (padded rows)
+  int last_flag;                   // split-K: this CTA completed the tile's sum
+  int pad;
+  union alignas(16) Scratch {
+    float xchg[2][2][kTileM];                   // up: [tile parity][column half][row] amax exchange
+    float red[kNumEpiWarps][32][kRedCols + 4];  // down: per-warp transpose buffer (padded rows), float4 access
+  } u;
+  int32_t row_tok[kTileM];         // up with split K: token of each tile row (-1 = no route)
   int32_t expert[kMaxBlocksSmem];  // expert of each plan block (cached at start)
+  uint8_t pairf[kMaxBlocksSmem];   // pair mode: bit 0 leads a pair, bit 1 has a partner
 };
 
-constexpr size_t kSmemBytes =
-    1024 + static_cast<size_t>(kStages) * (kABytes + kBBytes + sizeof(StageExtra)) + sizeof(SmemCtl);
+static_assert(offsetof(SmemCtl, u) % 16 == 0, "vector accesses to the transpose buffer need 16-byte alignment");
+static_assert(sizeof(SmemCtl) % 16 == 0, "control block size");
+
+template <bool kPair>
+constexpr size_t smem_bytes() {
+  return 1024 + static_cast<size_t>(Cfg<kPair>::kStages) * (kABytes + Cfg<kPair>::kBStage + sizeof(StageExtra)) +
+         sizeof(SmemCtl);
+}
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 
 struct GemmParams {
   const int32_t* expert_ids;
@@ -93,8 +115,8 @@ struct GemmParams {
   const int32_t* sorted_ids;   // up with gather4: plan (token of each row)
   const float* a_scale_t;      // [nkb, cap_pad]: scale of each plan slot per K slice
   const float4* w_scale_st;    // [nblocks, ntiles_n, nkb]: weight scales per tile and slice
-  const int32_t* slot_tok;     // down: [cap_pad] token per plan slot (-1 = pad)
-  const float* slot_w;         // down: [cap_pad] route weight x routed scale
+  const int32_t* slot_tok;     // [cap_pad] token per plan slot (-1 = pad)
+  const float* slot_w;         // [cap_pad] route weight x routed scale
   float* acc_out;              // down: [M, H]
   uint8_t* q_inter;            // up: [sorted_cap, I]
   float* s_inter_t;            // up: [I/128, cap_pad]
@@ -115,6 +137,10 @@ struct GemmParams {
   int a_gather4;               // up only: 1 = activation rows fetched by token with tile::gather4,
                                //          0 = rows already in plan order (2D boxes by plan slot)
   int block_major;             // tile order: 1 = all n tiles of a plan block together, 0 = n-tile major
+  int splits;                  // up only: K splits per tile (1 = none)
+  int ksplit;                  // K slices per split
+  float* usum;                 // up, splits > 1: [nblocks, ntiles_n, block_m, 256] zeroed partial sums
+  int32_t* ucnt;               // up, splits > 1: [nblocks, ntiles_n] zeroed arrival tickets
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -137,17 +163,22 @@ __device__ __forceinline__ int block_expert(const GemmParams& p, const SmemCtl* 
   return b < kMaxBlocksSmem ? ctl->expert[b] : p.expert_ids[b];
 }
 
-// Tile -> (plan block, n tile, expert); false if the tile has no work.
+// Tile -> (plan block, n tile, K split, expert); false if the tile has no
+// work.  In pair mode only blocks that lead a pair carry tiles.
+template <bool kPair>
 __device__ __forceinline__ bool tile_coords(const GemmParams& p, const SmemCtl* ctl, int64_t tile, int64_t nvalid,
-                                            int& b, int& t, int& e) {
+                                            int& b, int& t, int& sp, int& e) {
+  sp = static_cast<int>(tile % p.splits);
+  const int64_t bt = tile / p.splits;
   if (p.block_major) {
-    b = static_cast<int>(tile / p.ntiles_n);
-    t = static_cast<int>(tile % p.ntiles_n);
+    b = static_cast<int>(bt / p.ntiles_n);
+    t = static_cast<int>(bt % p.ntiles_n);
   } else {
-    b = static_cast<int>(tile % p.nblocks);
-    t = static_cast<int>(tile / p.nblocks);
+    b = static_cast<int>(bt % p.nblocks);
+    t = static_cast<int>(bt / p.nblocks);
   }
   if (b >= nvalid) return false;
+  if (kPair && !(ctl->pairf[b] & 1)) return false;
   e = block_expert(p, ctl, b);
   return e >= 0 && e < p.E;
 }
@@ -165,29 +196,108 @@ __device__ __forceinline__ void load_ids(const GemmParams& p, int b, int lane, i
   }
 }
 
-template <bool kUp>
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster.  Release at CTA scope
+// is enough for its one use (handing a TMEM buffer back after the reads have
+// completed); a cluster-scope release waits for the CTA's outstanding memory
+// traffic and costs microseconds under the operand stream.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// 2D tensor load whose completion is signalled on an mbarrier that may sit in
+// the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+template <bool kPair>
+__device__ __forceinline__ void tmem_alloc_k(uint32_t dst, uint32_t ncols) {
+  if (kPair)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+}
+template <bool kPair>
+__device__ __forceinline__ void tmem_relinquish_k() {
+  if (kPair)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+template <bool kPair>
+__device__ __forceinline__ void tmem_dealloc_k(uint32_t taddr, uint32_t ncols) {
+  if (kPair)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// The MMA of the pair: M = 256 (128 rows in each CTA), B split along N.
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the same mbarrier in both CTAs of the pair once every MMA issued
+// so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+template <bool kUp, bool kPair>
 __global__ void __launch_bounds__(kNumThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
+  using C = Cfg<kPair>;
+  constexpr int kStages = C::kStages;
+  constexpr int kBStage = C::kBStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  StageExtra* sX = reinterpret_cast<StageExtra*>(sB + kStages * kBBytes);
+  StageExtra* sX = reinterpret_cast<StageExtra*>(sB + kStages * kBStage);
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sX + kStages);
   volatile int* abort_flag = &ctl->abort_flag;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = kPair ? cluster_rank() : 0u;       // 0 = leader of the pair
+  // work is dealt per CTA, or per pair of CTAs (recomputed where used, to keep registers free)
+#define MOE_CTA_ID (kPair ? blockIdx.x / 2u : blockIdx.x)
+#define MOE_CTA_COUNT (kPair ? gridDim.x / 2u : gridDim.x)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1 + kNumEpiWarps);  // MMA commit + every epilogue warp
+      mbar_init(smem_u32(&ctl->xfull[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1 + kNumEpiWarps);  // MMA commit + every local epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctl->tempty[b]), kNumEpiWarps);
+      mbar_init(smem_u32(&ctl->tempty[b]), (kPair ? 2 : 1) * kNumEpiWarps);
     }
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -195,39 +305,60 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_k<kPair>(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish_k<kPair>();
   }
+  pdl_launch_dependents();
+  pdl_wait();
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
   if (nvalid > p.nblocks) nvalid = p.nblocks;
   const int64_t ncache = nvalid < kMaxBlocksSmem ? nvalid : kMaxBlocksSmem;
   for (int64_t b = threadIdx.x; b < ncache; b += blockDim.x) ctl->expert[b] = p.expert_ids[b];
+  if (kPair) {
+    __syncthreads();
+    // a block leads a pair when an even number of blocks of its expert
+    // precede it; its partner is the next block if it has the same expert
+    for (int64_t b = threadIdx.x; b < ncache; b += blockDim.x) {
+      const int e = ctl->expert[b];
+      int64_t run = 0;
+      while (b - run - 1 >= 0 && ctl->expert[b - run - 1] == e) ++run;
+      const bool lead = (run & 1) == 0;
+      const bool partner = lead && b + 1 < ncache && ctl->expert[b + 1] == e;
+      ctl->pairf[b] = static_cast<uint8_t>((lead ? 1 : 0) | (partner ? 2 : 0));
+    }
+  }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // the peer's copies and arrivals target initialised barriers
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int64_t total = p.nblocks * p.ntiles_n;
+  const int64_t total = p.nblocks * p.ntiles_n * p.splits;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
     bool ok = true;
-    int64_t tile = blockIdx.x;
-    int b = 0, t = 0, e = 0;
-    while (tile < total && !tile_coords(p, ctl, tile, nvalid, b, t, e)) tile += gridDim.x;
+    int64_t tile = MOE_CTA_ID;
+    int b = 0, t = 0, sp = 0, e = 0;
+    while (tile < total && !tile_coords<kPair>(p, ctl, tile, nvalid, b, t, sp, e)) tile += MOE_CTA_COUNT;
     // gather4 path: a tile's plan entries are read one tile ahead
     int ids[4] = {-1, -1, -1, -1};
-    if (kUp && p.a_gather4 && tile < total) load_ids(p, b, lane, ids);
+    if (kUp && !kPair && p.a_gather4 && tile < total) load_ids(p, b, lane, ids);
+    const uint32_t lead_full0 = kPair ? mapa_shared(smem_u32(&ctl->full[0]), 0) : smem_u32(&ctl->full[0]);
     while (tile < total && ok) {
-      int64_t ntile = tile + gridDim.x;
-      int nb = 0, nt = 0, ne = 0;
-      while (ntile < total && !tile_coords(p, ctl, ntile, nvalid, nb, nt, ne)) ntile += gridDim.x;
+      int64_t ntile = tile + MOE_CTA_COUNT;
+      int nb = 0, nt = 0, nsp = 0, ne = 0;
+      while (ntile < total && !tile_coords<kPair>(p, ctl, ntile, nvalid, nb, nt, nsp, ne)) ntile += MOE_CTA_COUNT;
+      // this CTA's plan block; in a pair the second CTA takes the partner block
+      const bool partner = kPair && (ctl->pairf[b] & 2);
+      const bool has_rows = !kPair || rank == 0 || partner;
+      const int mb = b + static_cast<int>(kPair && rank == 1 && partner ? 1 : 0);
       int tok[4] = {0, 0, 0, 0};
       bool mine = false;                 // this lane's four rows hold a route
-      uint32_t a_bytes = kABytes;
-      if (kUp && p.a_gather4) {
+      uint32_t a_bytes = has_rows ? kABytes : 0u;
+      if (kUp && !kPair && p.a_gather4) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const bool route = ids[i] >= 0 && ids[i] < p.R;
@@ -239,58 +370,81 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         a_bytes = 512u * static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, mine)));
         if (ntile < total) load_ids(p, nb, lane, ids);
       }
-      const int brow = e * p.b_rows + t * kTileN;
-      const int64_t slot0 = static_cast<int64_t>(b) * p.block_m;
-      for (int kb = 0; kb < p.nkb; ++kb) {
+      // the leader's barrier counts the operand bytes of both CTAs
+      const uint32_t op_bytes = kPair ? (kABytes + (partner ? kABytes : 0u) + 2u * kBStage) : a_bytes + kBStage;
+      const int brow = e * p.b_rows + t * kTileN + static_cast<int>(rank) * kBStage / kTileK;
+      const int64_t slot0 = static_cast<int64_t>(mb) * p.block_m;
+      const int kb0 = sp * p.ksplit;
+      const int kb1 = min(p.nkb, kb0 + p.ksplit);
+      for (int kb = kb0; kb < kb1; ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        const uint32_t full = smem_u32(&ctl->full[s]);
-        const bool tile_info = !kUp && kb == 0;
+        const uint32_t full = kPair ? lead_full0 + 8u * s : smem_u32(&ctl->full[s]);
+        const uint32_t xfull = smem_u32(&ctl->xfull[s]);
+        const bool tile_info = (!kUp || (!kPair && p.splits > 1)) && kb == kb0;
         const uint32_t extra = 512u + 16u + (tile_info ? 1024u : 0u);
-        if (lane == 0) mbar_arrive_expect_tx(full, a_bytes + kBBytes + extra);
+        if (lane == 0) {
+          if (!kPair || rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), op_bytes);
+          mbar_arrive_expect_tx(xfull, extra);
+        }
+        // the small side copies go first: queued behind the operand boxes
+        // they would land last and hold up the epilogue, which frees the stage
+        if (lane == 0) {
+          StageExtra* x = sX + s;
+          bulk_load(smem_u32(x->a_scale), p.a_scale_t + kb * p.cap_pad + slot0, 512u, xfull);
+          bulk_load(smem_u32(&x->w_scale), p.w_scale_st + (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb, 16u,
+                    xfull);
+          if (tile_info) {
+            bulk_load(smem_u32(x->tok), p.slot_tok + slot0, 512u, xfull);
+            bulk_load(smem_u32(x->weight), p.slot_w + slot0, 512u, xfull);
+          }
+        }
         __syncwarp();
         const uint32_t a_dst = smem_u32(sA + s * kABytes);
-        if (kUp && p.a_gather4) {
+        if (kUp && !kPair && p.a_gather4) {
           if (mine) tma_gather4(a_dst + 512u * lane, &tmA, full, kb * kTileK, tok[0], tok[1], tok[2], tok[3]);
-        } else if (lane == 0) {
-          tma_load_2d(a_dst, &tmA, full, kb * kTileK, b * p.block_m);
+        } else if (lane == 0 && has_rows) {
+          if (kPair)
+            tma_load_2d_pair(a_dst, &tmA, full, kb * kTileK, mb * p.block_m);
+          else
+            tma_load_2d(a_dst, &tmA, full, kb * kTileK, mb * p.block_m);
         }
         if (lane == 0) {
-          tma_load_2d(smem_u32(sB + s * kBBytes), &tmB, full, kb * kTileK, brow);
-          StageExtra* x = sX + s;
-          bulk_load(smem_u32(x->a_scale), p.a_scale_t + kb * p.cap_pad + slot0, 512u, full);
-          bulk_load(smem_u32(&x->w_scale), p.w_scale_st + (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb, 16u,
-                    full);
-          if (tile_info) {
-            bulk_load(smem_u32(x->tok), p.slot_tok + slot0, 512u, full);
-            bulk_load(smem_u32(x->weight), p.slot_w + slot0, 512u, full);
-          }
+          if (kPair)
+            tma_load_2d_pair(smem_u32(sB + s * kBStage), &tmB, full, kb * kTileK, brow);
+          else
+            tma_load_2d(smem_u32(sB + s * kBStage), &tmB, full, kb * kTileK, brow);
         }
         ++it;
       }
       tile = ntile;
       b = nb;
       t = nt;
+      sp = nsp;
       e = ne;
     }
     if (!ok && lane == 0) {
       // wind down: let the copies already issued land before the CTA exits
-      for (uint32_t j = (it > kStages ? it - kStages : 0); j < it; ++j)
-        drain_wait(smem_u32(&ctl->full[j % kStages]), (j / kStages) & 1u);
+      for (uint32_t j = (it > kStages ? it - kStages : 0); j < it; ++j) {
+        if (!kPair || rank == 0) drain_wait(smem_u32(&ctl->full[j % kStages]), (j / kStages) & 1u);
+        drain_wait(smem_u32(&ctl->xfull[j % kStages]), (j / kStages) & 1u);
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader of a pair)
+    if (lane == 0 && rank == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        int b, t, e;
-        if (!tile_coords(p, ctl, tile, nvalid, b, t, e)) continue;
-        for (int kb = 0; kb < p.nkb; ++kb) {
+      for (int64_t tile = MOE_CTA_ID; tile < total && ok; tile += MOE_CTA_COUNT) {
+        int b, t, sp, e;
+        if (!tile_coords<kPair>(p, ctl, tile, nvalid, b, t, sp, e)) continue;
+        const int kb0 = sp * p.ksplit;
+        const int kb1 = min(p.nkb, kb0 + p.ksplit);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           const uint32_t tb = it & 1u;
@@ -302,13 +456,24 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kABytes);
-          const uint32_t b0 = smem_u32(sB + s * kBBytes);
+          const uint32_t b0 = smem_u32(sB + s * kBStage);
           const uint32_t d = tmem_base + tb * kTileN;
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 32; ++kk)
-            umma_f8(d, sw128_kmajor_desc(a0 + 32u * kk), sw128_kmajor_desc(b0 + 32u * kk), kIdesc, kk > 0 ? 1u : 0u);
-          umma_commit(smem_u32(&ctl->empty[s]));
-          umma_commit(smem_u32(&ctl->tfull[tb]));
+          for (int kk = 0; kk < kTileK / 32; ++kk) {
+            if (kPair)
+              umma_f8_pair(d, sw128_kmajor_desc(a0 + 32u * kk), sw128_kmajor_desc(b0 + 32u * kk), C::kIdesc,
+                           kk > 0 ? 1u : 0u);
+            else
+              umma_f8(d, sw128_kmajor_desc(a0 + 32u * kk), sw128_kmajor_desc(b0 + 32u * kk), C::kIdesc,
+                      kk > 0 ? 1u : 0u);
+          }
+          if (kPair) {
+            umma_commit_pair(smem_u32(&ctl->empty[s]));
+            umma_commit_pair(smem_u32(&ctl->tfull[tb]));
+          } else {
+            umma_commit(smem_u32(&ctl->empty[s]));
+            umma_commit(smem_u32(&ctl->tfull[tb]));
+          }
           ++it;
         }
       }
@@ -321,21 +486,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
-    const bool rvalid = row < p.block_m;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t it = 0;
     int tcount = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int b, t, e;
-      if (!tile_coords(p, ctl, tile, nvalid, b, t, e)) {
-        if (warp == 2 && lane == 0 && t == 0 && static_cast<int64_t>(b) < nvalid) {
+    for (int64_t tile = MOE_CTA_ID; tile < total; tile += MOE_CTA_COUNT) {
+      int b, t, sp, e;
+      if (!tile_coords<kPair>(p, ctl, tile, nvalid, b, t, sp, e)) {
+        if (warp == 2 && lane == 0 && rank == 0 && t == 0 && sp == 0 && static_cast<int64_t>(b) < nvalid &&
+            (!kPair || (ctl->pairf[b] & 1))) {
           const int bad = block_expert(p, ctl, b);
           if (bad != -1) report(p.status, MOE_DEV_BAD_EXPERT);
         }
         continue;
       }
-      const int64_t slot = static_cast<int64_t>(b) * p.block_m + row;
       int tok = -1;
       float wr = 0.f;
 
@@ -343,14 +507,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
       for (int c = 0; c < 128; ++c) acc[c] = 0.f;
 
-      for (int kb = 0; kb < p.nkb; ++kb) {
+      const int kb0 = sp * p.ksplit;
+      const int kb1 = min(p.nkb, kb0 + p.ksplit);
+      for (int kb = kb0; kb < kb1; ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         const uint32_t tb = it & 1u;
         const uint32_t tph = (it >> 1) & 1u;
         // the slice's scales (and the tile's row data) arrive with the stage
         float s0 = 0.f, s1 = 0.f;
-        if (ok) ok = warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag);
+        if (ok) ok = warp_wait(smem_u32(&ctl->xfull[s]), ph, abort_flag);
         if (ok) {
           const StageExtra* x = sX + s;
           const float as = x->a_scale[row];
@@ -360,9 +526,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             s1 = __fmul_rn(as, ws.y);  // up block
           } else {
             s0 = __fmul_rn(as, half == 0 ? ws.x : ws.y);
-            if (kb == 0) {
+          }
+          if (kb == kb0) {
+            if (!kUp) {
               tok = x->tok[row];
               wr = x->weight[row];
+            } else if (!kPair && p.splits > 1) {
+              ctl->row_tok[row] = x->tok[row];  // read back at the tile end (keeps registers free)
             }
           }
         }
@@ -385,11 +555,58 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           tc_fence_before();
         }
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(smem_u32(&ctl->tempty[tb]));
+        if (ok && lane == 0) {
+          if (kPair && rank == 1)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[tb]), 0));
+          else
+            mbar_arrive(smem_u32(&ctl->tempty[tb]));
+        }
         ++it;
       }
 
-      if (kUp) {
+      // this CTA's plan block (in a pair the second CTA takes the partner
+      // block), its row validity and plan slot; evaluated where needed
+#define MOE_HAS_ROWS (!kPair || rank == 0 || (ctl->pairf[b] & 2))
+#define MOE_RVALID (MOE_HAS_ROWS && row < p.block_m)
+#define MOE_SLOT (static_cast<int64_t>(b + ((kPair && rank == 1) ? 1 : 0)) * p.block_m + row)
+      bool have = true;  // this CTA holds the tile's complete sum
+      if (kUp && !kPair && p.splits > 1) {
+        // split K: add this split's partial into the tile's zeroed sum; the
+        // split that arrives last reads the total back and finishes the tile
+        const bool live = ok && MOE_RVALID && ctl->row_tok[row] >= 0;
+        float* srow = p.usum + ((static_cast<int64_t>(b) * p.ntiles_n + t) * p.block_m + (live ? row : 0)) * kTileN +
+                      128 * half;
+        if (live) {
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) red_add_v4(srow + c, acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+        }
+        __threadfence();
+        named_barrier(1, 32 * kNumEpiWarps);
+        if (warp == 2 && lane == 0) {
+          int32_t* cnt = p.ucnt + static_cast<int64_t>(b) * p.ntiles_n + t;
+          const int old = ok ? atomicAdd(cnt, 1) : -1;
+          const bool last = old == p.splits - 1;
+          if (last) *cnt = 0;
+          ctl->last_flag = last ? 1 : 0;
+        }
+        named_barrier(1, 32 * kNumEpiWarps);
+        have = ctl->last_flag != 0;
+        if (have) {
+          __threadfence();
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(srow + c));
+              acc[c] = v.x;
+              acc[c + 1] = v.y;
+              acc[c + 2] = v.z;
+              acc[c + 3] = v.w;
+              *reinterpret_cast<float4*>(srow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+      }
+      if (kUp && have) {
         // SwiGLU on the 64 (gate, up) pairs this thread holds, then the
         // per-token 1x128 requant shared with the partner warp (other half).
         float amax = 0.f;
@@ -402,14 +619,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             amax = fmaxf(amax, fabsf(h));
           }
         }
-        ctl->xchg[tcount & 1][half][row] = amax;
+        ctl->u.xchg[tcount & 1][half][row] = amax;
         named_barrier(1, 32 * kNumEpiWarps);
-        amax = fmaxf(amax, ctl->xchg[tcount & 1][half ^ 1][row]);
+        amax = fmaxf(amax, ctl->u.xchg[tcount & 1][half ^ 1][row]);
         const float s = __fdiv_rn(amax, 448.0f);
         // h / s as h * (1/s): the two roundings can move a value across an
         // E4M3 rounding midpoint only when it lies within an ulp of it
         const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-        if (ok && rvalid) {
+        if (ok && MOE_RVALID) {
+          const int64_t slot = MOE_SLOT;
           uint32_t packed[16];
 #pragma unroll
           for (int w = 0; w < 16; ++w) {
@@ -431,39 +649,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (half == 0) p.dbg_s[slot * (p.I / 128) + t] = s;
           }
         }
-      } else {
+      } else if (!kUp) {
         const int hblk = 2 * t + half;
         if (ok && hblk < p.H / 128) {
           // rows of this warp: quarter*32 + r; lane l reduces row 8*i + l/4,
           // columns 4*(l%4) .. +3 of each 16-column chunk
-          const bool live = rvalid && tok >= 0;
+          const bool live = MOE_RVALID && tok >= 0;
           if (__any_sync(0xffffffffu, live)) {
-          float (*buf)[kRedCols + 4] = ctl->red[warp - 2];
-          const int sub = lane >> 2, c4 = 4 * (lane & 3);
-          int toks[4];
-          float* dst[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            toks[i] = __shfl_sync(0xffffffffu, live ? tok : -1, 8 * i + sub);
-            dst[i] = p.acc_out + static_cast<int64_t>(toks[i] < 0 ? 0 : toks[i]) * p.H + hblk * 128 + c4;
-          }
-#pragma unroll
-          for (int ch = 0; ch < 128 / kRedCols; ++ch) {
-#pragma unroll
-            for (int j = 0; j < kRedCols; j += 4)
-              *reinterpret_cast<float4*>(&buf[lane][j]) =
-                  make_float4(__fmul_rn(acc[ch * kRedCols + j], wr), __fmul_rn(acc[ch * kRedCols + j + 1], wr),
-                              __fmul_rn(acc[ch * kRedCols + j + 2], wr), __fmul_rn(acc[ch * kRedCols + j + 3], wr));
-            __syncwarp();
+            float(*buf)[kRedCols + 4] = ctl->u.red[warp - 2];
+            const int sub = lane >> 2, c4 = 4 * (lane & 3);
+            int toks[4];
+            float* dst[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              if (toks[i] >= 0) {
-                const float4 v = *reinterpret_cast<const float4*>(&buf[8 * i + sub][c4]);
-                red_add_v4(dst[i] + ch * kRedCols, v.x, v.y, v.z, v.w);
-              }
+              toks[i] = __shfl_sync(0xffffffffu, live ? tok : -1, 8 * i + sub);
+              dst[i] = p.acc_out + static_cast<int64_t>(toks[i] < 0 ? 0 : toks[i]) * p.H + hblk * 128 + c4;
             }
-            __syncwarp();
-          }
+#pragma unroll
+            for (int ch = 0; ch < 128 / kRedCols; ++ch) {
+#pragma unroll
+              for (int j = 0; j < kRedCols; j += 4)
+                *reinterpret_cast<float4*>(&buf[lane][j]) =
+                    make_float4(__fmul_rn(acc[ch * kRedCols + j], wr), __fmul_rn(acc[ch * kRedCols + j + 1], wr),
+                                __fmul_rn(acc[ch * kRedCols + j + 2], wr), __fmul_rn(acc[ch * kRedCols + j + 3], wr));
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (toks[i] >= 0) {
+                  const float4 v = *reinterpret_cast<const float4*>(&buf[8 * i + sub][c4]);
+                  red_add_v4(dst[i] + ch * kRedCols, v.x, v.y, v.z, v.w);
+                }
+              }
+              __syncwarp();
+            }
           }
         }
       }
@@ -473,9 +691,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // neither CTA leaves while the pair still touches its memory
   tc_fence_after();
   if (threadIdx.x == 0 && ctl->abort_flag) report(p.status, MOE_DEV_TIMEOUT);
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc_k<kPair>(tmem_base, kTmemCols);
+#undef MOE_CTA_ID
+#undef MOE_CTA_COUNT
+#undef MOE_HAS_ROWS
+#undef MOE_RVALID
+#undef MOE_SLOT
 }
 
 // Staging for the GEMM kernels (launch 0).  Part 1, one warp per plan slot
@@ -506,6 +730,8 @@ struct StageParams {
 };
 
 __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
@@ -588,6 +814,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ ou
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   for (; i + stride < n8; i += 2 * stride) {
     const int64_t j = i + stride;
     const uint4 o0 = o4[i], o1 = o4[j];
@@ -624,10 +852,14 @@ int64_t block_bound(int64_t R, int E, int block_m) {
   return ceil_div(R + nonempty * (block_m - 1), block_m);
 }
 
+// Split K is available when the gate/up GEMM has fewer tiles than a GB300
+// has SMs (decode-sized plans); the workspace then holds the partial sums.
+constexpr int64_t kSplitTileLimit = 256;
+
 struct WsLayout {
-  size_t acc_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, total;
+  size_t acc_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, usum_off, ucnt_off, total;
   int64_t cap_pad, nblocks;
-  bool pregather;
+  bool pregather, splitk;
 };
 
 WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64_t sorted_cap) {
@@ -653,8 +885,72 @@ WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64
   l.wsu_off = take(l.nblocks * nib * nkb * 16);
   l.wsd_off = take(l.nblocks * nh * nib * 16);
   l.a_off = take(l.pregather ? sorted_cap * H : 0);
+  l.splitk = l.nblocks * nib < kSplitTileLimit;
+  l.usum_off = take(l.splitk ? l.nblocks * nib * block_m * 256 * 4 : 0);
+  l.ucnt_off = take(l.splitk ? l.nblocks * nib * 4 : 0);
   l.total = off;
   return l;
+}
+
+// Launch with programmatic stream serialization (the kernel calls
+// pdl_wait), optionally as clusters of `cluster` CTAs.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Clusters of two CTAs that the GPU holds at once.  GPCs need not have an
+// even number of SMs, so this can be below SMs / 2; a persistent grid larger
+// than it would run its last clusters as a second wave.
+int max_pair_clusters(int device, int sms) {
+  static std::mutex mu;
+  static int cached[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[device] > 0) return cached[device];
+  int best = sms / 2;
+  for (int up = 0; up < 2; ++up) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(kNumThreads);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t err =
+        up ? cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<true, true>, &cfg)
+           : cudaOccupancyMaxActiveClusters(&n, moe_gemm_kernel<false, true>, &cfg);
+    if (err != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (n < best) best = n;
+  }
+  cached[device] = best;
+  return best;
 }
 
 bool set_smem_attrs(int device) {
@@ -662,11 +958,14 @@ bool set_smem_attrs(int device) {
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (done[device]) return true;
-  if (cudaFuncSetAttribute(moe_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess)
-    return false;
-  if (cudaFuncSetAttribute(moe_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess)
+  if (cudaFuncSetAttribute(moe_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<false>())) != cudaSuccess ||
+      cudaFuncSetAttribute(moe_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<false>())) != cudaSuccess ||
+      cudaFuncSetAttribute(moe_gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<true>())) != cudaSuccess ||
+      cudaFuncSetAttribute(moe_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<true>())) != cudaSuccess)
     return false;
   done[device] = true;
   return true;
@@ -688,6 +987,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   if (a->M < 0 || a->H < 128 || a->H % 128 || a->I < 128 || a->I % 128 || a->E < 1 || a->top_k < 1)
     return MOE_ERR_SHAPE;
   if (a->block_m < 8 || a->block_m > 128 || a->block_m % 8) return MOE_ERR_SHAPE;
+  if (a->tile_mode != MOE_TILE_AUTO && a->tile_mode != MOE_TILE_SINGLE && a->tile_mode != MOE_TILE_PAIR)
+    return MOE_ERR_SHAPE;
   if (a->blocks_cap < 1 || a->sorted_cap < a->blocks_cap * a->block_m) return MOE_ERR_CAPACITY;
   const int64_t R = a->M * a->top_k;
   if (R >= (int64_t(1) << 31) - 1 || static_cast<int64_t>(a->E) * 2 * a->I >= (int64_t(1) << 31) ||
@@ -728,22 +1029,31 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   uint8_t* a_sorted = wl.pregather ? ws + wl.a_off : nullptr;
 
   const int N = 2 * a->I;
+  int64_t nblocks = wl.nblocks;
+  if (nblocks > a->blocks_cap) nblocks = a->blocks_cap;
+  // CTA pairs (cta_group::2) need the activation rows in plan order and the
+  // expert and pair tables in shared memory.  Each SM then streams half of
+  // every weight tile, but per K slice the pair runs no faster than a single
+  // CTA: the slice's FP32 promotion in the epilogue, not the operand stream,
+  // paces the two TMEM buffers.  So the automatic choice stays single.
+  const bool want_pair = a->tile_mode == MOE_TILE_PAIR;
+  const int pair_clusters =
+      want_pair && wl.pregather && nblocks <= kMaxBlocksSmem ? max_pair_clusters(dev.device, dev.sms) : 0;
+  const bool pair = pair_clusters > 0;
+  const uint32_t wbox = pair ? kTileN / 2 : kTileN;
   CUtensorMap tm_a, tm_w13, tm_q, tm_w2;
   const CUresult ra = wl.pregather
                           ? encode_tensor_map_2d(&tm_a, a_sorted, a->H, a->sorted_cap, a->H, 128, 128,
                                                  CU_TENSOR_MAP_SWIZZLE_128B)
                           : encode_tensor_map_2d(&tm_a, a->a, a->H, a->M, a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (ra != CUDA_SUCCESS ||
-      encode_tensor_map_2d(&tm_w13, a->w13, a->H, static_cast<uint64_t>(a->E) * N, a->H, 128, 256,
+      encode_tensor_map_2d(&tm_w13, a->w13, a->H, static_cast<uint64_t>(a->E) * N, a->H, 128, wbox,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tensor_map_2d(&tm_q, q_inter, a->I, a->sorted_cap, a->I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) !=
           CUDA_SUCCESS ||
-      encode_tensor_map_2d(&tm_w2, a->w2, a->I, static_cast<uint64_t>(a->E) * a->H, a->I, 128, 256,
+      encode_tensor_map_2d(&tm_w2, a->w2, a->I, static_cast<uint64_t>(a->E) * a->H, a->I, 128, wbox,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
-
-  int64_t nblocks = wl.nblocks;
-  if (nblocks > a->blocks_cap) nblocks = a->blocks_cap;
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
@@ -774,8 +1084,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     sp.routed_scale = a->routed_scale;
     int64_t sgrid = ceil_div(nblocks * a->block_m, 8);
     if (sgrid > static_cast<int64_t>(dev.sms) * 8) sgrid = static_cast<int64_t>(dev.sms) * 8;
-    stage_kernel<<<static_cast<unsigned>(sgrid), 256, 0, stream>>>(sp);
-    MOE_CUDA_TRY(cudaGetLastError());
+    MOE_CUDA_TRY(launch_pdl(stage_kernel, dim3(static_cast<unsigned>(sgrid)), dim3(256), 0, stream, 1, sp));
 
     GemmParams p{};
     p.expert_ids = a->expert_ids;
@@ -803,10 +1112,34 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     up.b_rows = N;
     up.a_gather4 = wl.pregather ? 0 : 1;
     up.block_major = 1;
-    const int64_t up_tiles = nblocks * up.ntiles_n;
-    const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
-    moe_gemm_kernel<true><<<up_grid, kNumThreads, kSmemBytes, stream>>>(tm_a, tm_w13, up);
-    MOE_CUDA_TRY(cudaGetLastError());
+    up.slot_tok = slot_tok;
+    up.slot_w = slot_w;
+    // split K when the tiles cannot fill the GPU (decode): each split streams
+    // a share of the weights, the last one to finish applies SwiGLU
+    up.splits = 1;
+    up.ksplit = up.nkb;
+    const int64_t base_tiles = nblocks * up.ntiles_n;
+    if (!pair && wl.splitk && base_tiles < dev.sms) {
+      int want = static_cast<int>(dev.sms / base_tiles);
+      if (want > up.nkb) want = up.nkb;
+      if (want > 1) {
+        up.ksplit = static_cast<int>(ceil_div(up.nkb, want));
+        up.splits = static_cast<int>(ceil_div(up.nkb, up.ksplit));
+        up.usum = reinterpret_cast<float*>(ws + wl.usum_off);
+        up.ucnt = reinterpret_cast<int32_t*>(ws + wl.ucnt_off);
+      }
+    }
+    const int64_t up_tiles = base_tiles * up.splits;
+    if (pair) {
+      int64_t clusters = ceil_div(up_tiles, 2);
+      if (clusters > pair_clusters) clusters = pair_clusters;
+      MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, true>, dim3(static_cast<unsigned>(2 * clusters)),
+                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_a, tm_w13, up));
+    } else {
+      const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
+      MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false>, dim3(up_grid), dim3(kNumThreads), smem_bytes<false>(),
+                              stream, 1, tm_a, tm_w13, up));
+    }
     if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
 
     GemmParams dn = p;
@@ -820,10 +1153,19 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     dn.b_rows = a->H;
     dn.a_gather4 = 0;
     dn.block_major = 0;
+    dn.splits = 1;
+    dn.ksplit = dn.nkb;
     const int64_t dn_tiles = nblocks * dn.ntiles_n;
-    const int dn_grid = static_cast<int>(dn_tiles < dev.sms ? dn_tiles : dev.sms);
-    moe_gemm_kernel<false><<<dn_grid, kNumThreads, kSmemBytes, stream>>>(tm_q, tm_w2, dn);
-    MOE_CUDA_TRY(cudaGetLastError());
+    if (pair) {
+      int64_t clusters = ceil_div(dn_tiles, 2);
+      if (clusters > pair_clusters) clusters = pair_clusters;
+      MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<false, true>, dim3(static_cast<unsigned>(2 * clusters)),
+                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_q, tm_w2, dn));
+    } else {
+      const int dn_grid = static_cast<int>(dn_tiles < dev.sms ? dn_tiles : dev.sms);
+      MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<false, false>, dim3(dn_grid), dim3(kNumThreads), smem_bytes<false>(),
+                              stream, 1, tm_q, tm_w2, dn));
+    }
   } else if (ev) {
     MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
   }
@@ -832,8 +1174,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   const int64_t n8 = a->M * a->H / 8;
   int64_t fgrid = ceil_div(n8, 256);
   if (fgrid > static_cast<int64_t>(dev.sms) * 16) fgrid = static_cast<int64_t>(dev.sms) * 16;
-  finalize_kernel<<<static_cast<unsigned>(fgrid), 256, 0, stream>>>(a->out, acc, n8);
-  MOE_CUDA_TRY(cudaGetLastError());
+  MOE_CUDA_TRY(
+      launch_pdl(finalize_kernel, dim3(static_cast<unsigned>(fgrid)), dim3(256), 0, stream, 1, a->out, acc, n8));
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
   return MOE_OK;
 }

@@ -183,7 +183,21 @@ typedef struct moe_fwd_args {
                                               `stream` before the gate/up kernel, after it,
                                               after the down kernel and after the finalize
                                               kernel (per-kernel timing; no effect if NULL)  */
+  int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
 } moe_fwd_args;
+
+/* tile_mode values.  Every mode computes the same result.
+ *   MOE_TILE_AUTO   the library chooses (currently always one CTA per tile).
+ *   MOE_TILE_SINGLE one CTA per 128-row tile (cta_group::1 MMAs).
+ *   MOE_TILE_PAIR   two CTAs of a cluster per pair of plan blocks of one
+ *                   expert (cta_group::2, M = 256): each CTA streams half of
+ *                   the weight tile.  Used where the plan qualifies (activation
+ *                   rows copied into plan order and at most 1024 plan blocks),
+ *                   otherwise the forward falls back to MOE_TILE_SINGLE.
+ * Any other value returns MOE_ERR_SHAPE. */
+#define MOE_TILE_AUTO 0
+#define MOE_TILE_SINGLE 1
+#define MOE_TILE_PAIR 2
 
 /* Workspace bytes the forward needs (host-only; 0 for invalid sizes).  The
  * workspace holds an FP32 [M, H] route accumulator, the requantised

@@ -89,6 +89,10 @@ def test_forward_host_validation_without_gpu(lib):
     a.block_m = 256
     assert f(ctypes.byref(a), None) == 2                         # block_m > 128
     a.block_m = 64
+    for bad in (-1, 3):
+        a.tile_mode = bad
+        assert f(ctypes.byref(a), None) == 2                     # unknown tile mode
+    a.tile_mode = 2
     a.sorted_cap = 639
     assert f(ctypes.byref(a), None) == 4                         # capacity
     a.sorted_cap = 640

@@ -24,12 +24,12 @@ def _load():
     L.load()
 
 
-def _run(prob, debug=True):
+def _run(prob, debug=True, tile_mode=L.TILE_AUTO):
     cap = prob.sorted_ids.numel()
     dq = torch.zeros(cap, prob.cfg.I, dtype=torch.uint8, device="cuda") if debug else None
     ds = torch.zeros(cap, prob.cfg.I // 128, dtype=torch.float32, device="cuda") if debug else None
     prob.run_plan()
-    prob.run_forward(prob.fwd_args(dq, ds))
+    prob.run_forward(prob.fwd_args(dq, ds, tile_mode=tile_mode))
     torch.cuda.synchronize()
     return dq, ds
 
@@ -105,11 +105,10 @@ FULL = {
 }
 
 
-@pytest.mark.parametrize("name", list(FULL))
-def test_forward_full_size_sampled(name):
+def _full_size(name, tile_mode):
     cfg = W.CONFIGS[name]
     prob = DeviceProblem(cfg)
-    dq, ds = _run(prob)
+    dq, ds = _run(prob, tile_mode=tile_mode)
     n = FULL[name]
     if n is None:
         tokens = np.arange(cfg.M)
@@ -123,6 +122,48 @@ def test_forward_full_size_sampled(name):
         tokens = np.unique(np.concatenate([tokens, masked[:1], zero[:1]]))
     _check(prob, tokens, dq, ds, "full")
     assert int(prob.status.item()) == 0
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_forward_full_size_sampled(name):
+    _full_size(name, L.TILE_AUTO)
+
+
+# ------------------------------------------------------------------ CTA pairs (cta_group::2)
+
+# Plans with the activation rows in plan order qualify for CTA pairs: blocks
+# with a partner of the same expert (hot experts), lone blocks (the pair's
+# second CTA idles), block_m < 128 (a 128-row box spans several blocks) and
+# H % 256 == 128 (a half-empty last weight tile).
+PAIR_SMALL = [n for n in SMALL if n != "tiny"]
+
+
+@pytest.mark.parametrize("name", PAIR_SMALL)
+def test_forward_small_cta_pairs(name):
+    prob = DeviceProblem(SMALL[name])
+    dq, ds = _run(prob, tile_mode=L.TILE_PAIR)
+    _check(prob, np.arange(prob.cfg.M), dq, ds, "pairs")
+    assert int(prob.status.item()) == 0
+
+
+@pytest.mark.parametrize("name", ["prefill_1024", "prefill_8192", "skewed", "large"])
+def test_forward_full_size_cta_pairs(name):
+    _full_size(name, L.TILE_PAIR)
+
+
+def test_forward_modes_agree():
+    """Single CTAs and CTA pairs give the same intermediate codes and outputs
+    up to FP32 summation order."""
+    cfg = SMALL["hot_many_blocks"]
+    outs = []
+    for mode in (L.TILE_SINGLE, L.TILE_PAIR):
+        prob = DeviceProblem(cfg)
+        dq, _ = _run(prob, tile_mode=mode)
+        outs.append((prob.out.float().cpu(), dq.cpu().numpy()))
+    (o1, q1), (o2, q2) = outs
+    assert torch.allclose(o1, o2, rtol=1e-2, atol=1e-2)
+    nd, nf = code_diffs(q1, q2)
+    assert nf == 0 and nd <= max(1, CODE_DIFF_FRAC * q1.size)
 
 
 # ------------------------------------------------------------------ semantics
