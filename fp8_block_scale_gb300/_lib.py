@@ -207,13 +207,18 @@ def make_fwd_args(a, a_scale, w13, w13_scale, w2, w2_scale, topk_weights, sorted
     return args
 
 
+PROFILE_EVENTS = 5  # before staging, after staging, after gate/up, after down, after finalize
+
+
 def set_profile_events(args, events):
-    """Attach 4 recorded torch.cuda.Event objects (or None) to a moe_fwd_args."""
+    """Attach 5 recorded torch.cuda.Event objects (or None) to a moe_fwd_args."""
     if events is None:
         args.profile_events = None
         args._events_keepalive = None
         return
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    if len(events) != PROFILE_EVENTS:
+        raise ValueError(f"need {PROFILE_EVENTS} events")
+    arr = (ctypes.c_void_p * PROFILE_EVENTS)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     args._events_keepalive = arr
     args.profile_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
 

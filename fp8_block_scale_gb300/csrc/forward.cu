@@ -546,10 +546,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t v[16];
             tmem_ld_32x32b_x16(lane_base + tb * kTileN + 128u * half + 16u * ch, v);
             tmem_wait_ld();
+            // packed FP32 FMAs, two columns each (same rounding as two fmaf)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 16; i += 2) {
               const float sc = (kUp && (i & 8)) ? s1 : s0;  // up kernel: gate columns 0-7, up columns 8-15
-              acc[16 * ch + i] = fmaf(__uint_as_float(v[i]), sc, acc[16 * ch + i]);
+              const float2 r = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                          make_float2(sc, sc), make_float2(acc[16 * ch + i], acc[16 * ch + i + 1]));
+              acc[16 * ch + i] = r.x;
+              acc[16 * ch + i + 1] = r.y;
             }
           }
           tc_fence_before();
@@ -1085,6 +1089,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     int64_t sgrid = ceil_div(nblocks * a->block_m, 8);
     if (sgrid > static_cast<int64_t>(dev.sms) * 8) sgrid = static_cast<int64_t>(dev.sms) * 8;
     MOE_CUDA_TRY(launch_pdl(stage_kernel, dim3(static_cast<unsigned>(sgrid)), dim3(256), 0, stream, 1, sp));
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
 
     GemmParams p{};
     p.expert_ids = a->expert_ids;
@@ -1140,7 +1145,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false>, dim3(up_grid), dim3(kNumThreads), smem_bytes<false>(),
                               stream, 1, tm_a, tm_w13, up));
     }
-    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[2], stream));
 
     GemmParams dn = p;
     dn.a_scale_t = s_inter_t;
@@ -1168,15 +1173,16 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     }
   } else if (ev) {
     MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
+    MOE_CUDA_TRY(cudaEventRecord(ev[2], stream));
   }
-  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[2], stream));
+  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
 
   const int64_t n8 = a->M * a->H / 8;
   int64_t fgrid = ceil_div(n8, 256);
   if (fgrid > static_cast<int64_t>(dev.sms) * 16) fgrid = static_cast<int64_t>(dev.sms) * 16;
   MOE_CUDA_TRY(
       launch_pdl(finalize_kernel, dim3(static_cast<unsigned>(fgrid)), dim3(256), 0, stream, 1, a->out, acc, n8));
-  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
+  if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[4], stream));
   return MOE_OK;
 }
 

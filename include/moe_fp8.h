@@ -179,10 +179,12 @@ typedef struct moe_fwd_args {
   int32_t top_k;
   int32_t block_m;
   float routed_scale;                      /* routed scaling factor (1.0 = none)            */
-  void* const* profile_events;             /* nullable: 4 cudaEvent_t handles, recorded on
-                                              `stream` before the gate/up kernel, after it,
-                                              after the down kernel and after the finalize
-                                              kernel (per-kernel timing; no effect if NULL)  */
+  void* const* profile_events;             /* nullable: 5 cudaEvent_t handles, recorded on
+                                              `stream` before the staging kernel, after it,
+                                              after the gate/up kernel, after the down kernel
+                                              and after the finalize kernel (per-kernel
+                                              timing; events between the launches keep them
+                                              from overlapping; no effect if NULL)           */
   int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
 } moe_fwd_args;
 
