@@ -727,6 +727,8 @@ struct StageParams {
   float* slot_w;              // [cap_pad]
   float4* wsu;                // [nblocks, I/128, H/128]
   float4* wsd;                // [nblocks, ceil(H/256), I/128]
+  float4* acc;                // [M * H / 4] route accumulator, zeroed here for the down kernel
+  int64_t acc_n4;
   int64_t nblocks;
   int64_t cap_pad;
   int R, top_k, block_m, E, H, I;
@@ -736,6 +738,15 @@ struct StageParams {
 __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   pdl_launch_dependents();
   pdl_wait();
+  // Clear the route accumulator for this forward's down kernel (which starts
+  // after this grid completes).  Only after the wait: the previous forward's
+  // finalize may still be reading it.
+  {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < p.acc_n4; i += stride)
+      __stcs(p.acc + i, z);
+  }
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
@@ -796,7 +807,7 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   }
 }
 
-// out = bf16_rn(f32(out) + acc); acc = 0.  Eight elements per thread.
+// out = bf16_rn(f32(out) + acc).  Eight elements per thread.
 __device__ __forceinline__ uint4 add_bf16x8(uint4 o, float4 a0, float4 a1) {
   const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
   uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
@@ -811,11 +822,13 @@ __device__ __forceinline__ uint4 add_bf16x8(uint4 o, float4 a0, float4 a1) {
   return o;
 }
 
-// Two groups of eight per iteration, all loads issued before any store.
-__global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ out, float* __restrict__ acc, int64_t n8) {
+// Two groups of eight per iteration, all loads issued before any store.  The
+// accumulator is left as it is: the next forward's staging kernel clears it
+// (rewriting the lines just read here cost more than the rest of the pass).
+__global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ out, const float* __restrict__ acc,
+                                                       int64_t n8) {
   uint4* o4 = reinterpret_cast<uint4*>(out);
-  float4* a4 = reinterpret_cast<float4*>(acc);
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* a4 = reinterpret_cast<const float4*>(acc);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   pdl_launch_dependents();
@@ -823,19 +836,14 @@ __global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ ou
   for (; i + stride < n8; i += 2 * stride) {
     const int64_t j = i + stride;
     const uint4 o0 = o4[i], o1 = o4[j];
-    const float4 a0 = a4[2 * i], a1 = a4[2 * i + 1], b0 = a4[2 * j], b1 = a4[2 * j + 1];
-    a4[2 * i] = z;
-    a4[2 * i + 1] = z;
-    a4[2 * j] = z;
-    a4[2 * j + 1] = z;
+    const float4 a0 = __ldcs(a4 + 2 * i), a1 = __ldcs(a4 + 2 * i + 1), b0 = __ldcs(a4 + 2 * j),
+                 b1 = __ldcs(a4 + 2 * j + 1);
     o4[i] = add_bf16x8(o0, a0, a1);
     o4[j] = add_bf16x8(o1, b0, b1);
   }
   if (i < n8) {
     const uint4 o0 = o4[i];
-    const float4 a0 = a4[2 * i], a1 = a4[2 * i + 1];
-    a4[2 * i] = z;
-    a4[2 * i + 1] = z;
+    const float4 a0 = __ldcs(a4 + 2 * i), a1 = __ldcs(a4 + 2 * i + 1);
     o4[i] = add_bf16x8(o0, a0, a1);
   }
 }
@@ -1077,6 +1085,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     sp.slot_w = slot_w;
     sp.wsu = wsu;
     sp.wsd = wsd;
+    sp.acc = reinterpret_cast<float4*>(acc);
+    sp.acc_n4 = a->M * a->H / 4;
     sp.nblocks = nblocks;
     sp.cap_pad = wl.cap_pad;
     sp.R = static_cast<int>(R);

@@ -3,7 +3,8 @@
 // "Public contract and review fixes": sorted_token_ids holds
 // expert_ids.numel() * block_m slots).
 //
-// Deterministic three-launch counting sort:
+// Deterministic counting sort.  Up to kSmallRoutes routes (decode) it runs
+// as one CTA in one launch (plan_small_kernel); above that in three:
 //   1. rank:    each CTA takes a chunk of kChunk routes, computes every route's
 //               stable rank among same-expert routes of its chunk (warp
 //               match + per-warp histograms in shared memory) and the chunk's
@@ -22,6 +23,9 @@ constexpr int kChunk = 512;  // routes per CTA in the rank/scatter launches (one
 constexpr int kChunkWarps = kChunk / 32;
 constexpr int kScanThreads = 1024;
 constexpr int kMaxExperts = 2048;
+constexpr int kSmallRoutes = kScanThreads;  // one route per thread of the single-CTA plan
+constexpr int kSmallMaxExperts = 1024;      // its per-warp histograms: 32 x E ints of shared memory
+constexpr int kScanBatch = 8;               // chunk counts in flight per lane and expert
 
 struct PlanWs {
   int32_t* counts;  // [E, chunks]: per-chunk counts, then bases inside the expert
@@ -91,30 +95,66 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem /* 32 ints */) 
   return res;
 }
 
+// Pad sentinels (R) after each expert's routes and the expert of each of its
+// blocks: a warp per expert, lanes over the slots.
+__device__ void fill_pads(int E, int block_m, int64_t R, const int* totals, const int* seg, int32_t* sorted_ids,
+                          int32_t* expert_ids) {
+  const int lane = threadIdx.x % 32;
+  for (int e = threadIdx.x / 32; e < E; e += blockDim.x / 32) {
+    const int st = seg[e], tot = totals[e];
+    const int end = st + (tot + block_m - 1) / block_m * block_m;
+    for (int q = st + tot + lane; q < end; q += 32) sorted_ids[q] = static_cast<int32_t>(R);
+    for (int b = st / block_m + lane; b < end / block_m; b += 32) expert_ids[b] = e;
+  }
+}
+
 __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int E, int block_m, int nchunks, PlanWs ws,
                                                                   int32_t* sorted_ids, int32_t* expert_ids,
                                                                   int32_t* num_post_padded) {
   __shared__ int scan_smem[33];
   __shared__ int totals[kMaxExperts];
+  __shared__ int seg[kMaxExperts];
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   // 1. one warp per expert: exclusive scan of its chunk counts (bases inside
-  //    the expert) and the expert's total
-  for (int e = warp; e < E; e += kScanThreads / 32) {
-    int32_t* row = ws.counts + static_cast<int64_t>(e) * nchunks;
-    int carry = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nchunks ? row[c] : 0;
-      int inc = v;
+  //    the expert) and the expert's total.  A warp takes two experts at a
+  //    time and loads up to kScanBatch x 32 counts of each before scanning,
+  //    so the loads overlap instead of paying one latency per 32 chunks.
+  constexpr int kWarps = kScanThreads / 32;
+  for (int e0 = warp; e0 < E; e0 += 2 * kWarps) {
+    const int ee[2] = {e0, e0 + kWarps};
+    int carry[2] = {0, 0};
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * kScanBatch) {
+      int v[2][kScanBatch];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += n;
+      for (int x = 0; x < 2; ++x) {
+        const int32_t* row = ws.counts + static_cast<int64_t>(ee[x] < E ? ee[x] : 0) * nchunks;
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+          const int c = c0 + 32 * j + lane;
+          v[x][j] = (ee[x] < E && c < nchunks) ? row[c] : 0;
+        }
       }
-      if (c < nchunks) row[c] = carry + inc - v;
-      carry += __shfl_sync(0xffffffffu, inc, 31);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (ee[x] >= E) continue;
+        int32_t* row = ws.counts + static_cast<int64_t>(ee[x]) * nchunks;
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+          const int c = c0 + 32 * j + lane;
+          int inc = v[x][j];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += n;
+          }
+          if (c < nchunks) row[c] = carry[x] + inc - v[x][j];
+          carry[x] += __shfl_sync(0xffffffffu, inc, 31);
+        }
+      }
     }
-    if (lane == 0) totals[e] = carry;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (lane == 0 && ee[x] < E) totals[ee[x]] = carry[x];
   }
   __syncthreads();
   // 2. pad every expert to block_m and scan the experts
@@ -130,17 +170,19 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
   }
   int P = 0;
   int start = block_exclusive_scan(mine, &P, scan_smem);
-  // 3. segment starts, pad sentinels, block experts, P
+  // 3. segment starts; then a warp per expert writes its pad sentinels and
+  //    block experts (one slot per lane); P
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = threadIdx.x * kPer + i;
     if (e < E) {
       ws.seg[e] = start;
-      for (int s = start + total[i]; s < start + padded[i]; ++s) sorted_ids[s] = static_cast<int32_t>(R);
-      for (int b = start / block_m; b < (start + padded[i]) / block_m; ++b) expert_ids[b] = e;
+      seg[e] = start;
     }
     start += padded[i];
   }
+  __syncthreads();
+  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids);
   if (threadIdx.x == 0) *num_post_padded = P;
 }
 
@@ -153,6 +195,64 @@ __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, i
   const int e = load_id(ids, id_bits, r, E);
   const int base = ws.seg[e] + ws.counts[static_cast<int64_t>(e) * ws.nchunks + blockIdx.x];
   sorted_ids[base + rk] = static_cast<int32_t>(r);
+}
+
+// The whole plan in one CTA for R <= kSmallRoutes and E <= kSmallMaxExperts:
+// one route per thread, ranked by a warp match plus per-warp expert
+// histograms, then the padded expert scan and the scatter.  Same bytes as the
+// three-launch path (a stable counting sort).
+__global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* ids, int id_bits, int64_t R, int E,
+                                                                   int block_m, int32_t* sorted_ids,
+                                                                   int32_t* expert_ids, int32_t* num_post_padded) {
+  extern __shared__ int32_t wh[];  // [32][E]: per-warp counts, then their exclusive prefix over warps
+  __shared__ int scan_smem[33];
+  __shared__ int totals[kSmallMaxExperts];
+  __shared__ int seg[kSmallMaxExperts];
+  constexpr int kWarps = kScanThreads / 32;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int r = threadIdx.x;
+  const int e = r < R ? load_id(ids, id_bits, r, E) : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned below = peers & ((1u << lane) - 1u);
+  const int in_warp = __popc(below);
+  if (e >= 0 && below == 0) wh[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = wh[w * E + x];
+      wh[w * E + x] = run;
+      run += v;
+    }
+    totals[x] = run;
+  }
+  __syncthreads();
+  // padded expert lengths, scanned (the same steps as plan_scan_kernel)
+  constexpr int kPer = kSmallMaxExperts / kScanThreads;  // 1
+  int total[kPer], padded[kPer];
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int x = threadIdx.x * kPer + i;
+    total[i] = x < E ? totals[x] : 0;
+    padded[i] = (total[i] + block_m - 1) / block_m * block_m;
+    mine += padded[i];
+  }
+  int P = 0;
+  int start = block_exclusive_scan(mine, &P, scan_smem);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int x = threadIdx.x * kPer + i;
+    if (x < E) seg[x] = start;
+    start += padded[i];
+  }
+  if (threadIdx.x == 0) *num_post_padded = P;
+  __syncthreads();
+  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids);
+  if (e >= 0) sorted_ids[seg[e] + wh[warp * E + e] + in_warp] = static_cast<int32_t>(r);
 }
 
 size_t plan_ws_bytes(int64_t R, int E, int64_t* nchunks_out) {
@@ -208,7 +308,16 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
   if (!attr_set[dev.device]) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(plan_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChunkWarps * kMaxExperts * 4));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(plan_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (kScanThreads / 32) * kSmallMaxExperts * 4));
     attr_set[dev.device] = true;
+  }
+  if (R <= kSmallRoutes && E <= kSmallMaxExperts) {
+    const size_t small_smem = static_cast<size_t>(kScanThreads / 32) * E * sizeof(int32_t);
+    plan_small_kernel<<<1, kScanThreads, small_smem, stream>>>(topk_ids, id_bits, R, E, block_m, sorted_token_ids,
+                                                                expert_ids, num_tokens_post_padded);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
   }
   if (R > 0) {
     plan_rank_kernel<<<static_cast<unsigned>(nchunks), kChunk, smem, stream>>>(topk_ids, id_bits, R, E, ws);

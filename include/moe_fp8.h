@@ -211,7 +211,10 @@ size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int
                                   int64_t sorted_cap);
 
 /* Zero a forward workspace (async).  A workspace must be zeroed once before
- * its first forward; every forward returns it to the zeroed state.  Two
+ * its first forward; every forward leaves it ready for the next (the parts
+ * that must be zero on entry are returned to zero; the FP32 route
+ * accumulator, the first M * H * 4 bytes, is scratch the forward clears
+ * itself and leaves holding the last call's sums).  Two
  * forwards that share a workspace must not run concurrently. */
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
 

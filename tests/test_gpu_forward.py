@@ -168,16 +168,20 @@ def test_forward_modes_agree():
 
 # ------------------------------------------------------------------ semantics
 
-def test_forward_accumulates_and_leaves_workspace_zeroed():
+def test_forward_accumulates_and_reuses_its_workspace():
+    """out accumulates across calls; the route accumulator at the start of the
+    workspace is scratch the forward clears itself (here it holds huge values
+    before the second call), and the split-K sums (this plan splits K) are
+    back to zero after each call."""
     cfg = SMALL["ragged_bm64"]
     prob = DeviceProblem(cfg)
     _run(prob, debug=False)
     once = prob.out.float().clone()
+    acc_bytes = cfg.M * cfg.H * 4
+    prob.workspace[:acc_bytes].fill_(0x7F)
     prob.run_forward()
     torch.cuda.synchronize()
     twice = prob.out.float()
-    acc_bytes = cfg.M * cfg.H * 4
-    assert int(prob.workspace[:acc_bytes].view(torch.int32).abs().sum().item()) == 0
     delta1 = once - prob.out_prior.float()
     delta2 = twice - once
     rel = (delta2 - delta1).norm() / delta1.norm()

@@ -119,7 +119,8 @@ def test_plan_bit_exact_configs(name):
     _check_plan(r.topk_ids.to(torch.int64).numpy(), cfg.E, cfg.block_m, cfg.id_dtype)
 
 
-@pytest.mark.parametrize("case", ["all_masked", "out_of_range", "one_expert", "bm8", "bm1024", "int64", "hot"])
+@pytest.mark.parametrize("case", ["all_masked", "out_of_range", "one_expert", "bm8", "bm1024", "int64", "hot",
+                                  "r1024", "r1025", "e1024", "e1025", "e2048"])
 def test_plan_bit_exact_edges(case):
     rng = np.random.default_rng(11)
     E, bm, dt = 64, 64, torch.int32
@@ -140,6 +141,13 @@ def test_plan_bit_exact_edges(case):
     elif case == "int64":
         dt = torch.int64
         ids = rng.integers(-1, E, size=(123, 5))
+    elif case == "r1024":  # the largest plan the single-CTA path takes
+        ids = rng.integers(-1, E, size=(256, 4))
+    elif case == "r1025":  # one route more: the three-launch path
+        ids = rng.integers(-1, E, size=(205, 5))
+    elif case in ("e1024", "e1025", "e2048"):  # expert counts around the single-CTA limit, and the maximum
+        E = int(case[1:])
+        ids = rng.integers(-1, E, size=(90, 7))
     else:  # one expert takes most routes, spanning many blocks and chunks
         ids = np.where(rng.random((3000, 4)) < 0.7, 3, rng.integers(0, E, size=(3000, 4)))
     _check_plan(ids, E, bm, dt)
