@@ -15,6 +15,7 @@ a bounded token sample of the same workload instead.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -348,6 +349,25 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x, dist, device):
+    """The maximum of x over all ranks (x itself when not distributed).  A NaN
+    on any rank (a failed measurement) makes the result NaN: a MAX reduction
+    alone would drop it."""
+    if dist is None:
+        return float(x)
+    import torch
+    x = float(x)
+    t = torch.tensor([-math.inf if x != x else x, 1.0 if x != x else 0.0], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float("nan") if t[1].item() > 0 else float(t[0].item())
+
+
+def job_tflops(flop_per_rank, world, step_ms):
+    """Whole-job throughput: the FLOPs all ranks processed (each rank runs its
+    own batch of the workload) over the slowest rank's step time."""
+    return flop_per_rank * world / (step_ms * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world, dist):
     import torch
     from fp8_block_scale_gb300 import _lib as L
@@ -367,19 +387,11 @@ def run_ours(args, rank, world, dist):
     res = measure(prob, args.steps, args.warmup, flush, dist, ClockSampler(dev) if rank == 0 else None)
 
     # max over ranks of the timed interval
-    step_ms = res["step_ms"]
-    if dist is not None:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    total_flop = w["total"]["flop"] * world
-    value = total_flop / (step_ms * 1e-3) / 1e12
+    step_ms = max_over_ranks(res["step_ms"], dist, "cuda")
+    value = job_tflops(w["total"]["flop"], world, step_ms)
 
     e2e_ms, h2d, d2h = (float("nan"), 0, 0) if args.no_e2e else measure_e2e(prob, max(3, args.steps // 2), 2)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     if rank != 0:
         return
 
@@ -423,7 +435,7 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
                    "reasons": clocks.get("reasons", [])},
-        "e2e": {"value": w["total"]["flop"] * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tflops(w["total"]["flop"], world, e2e_ms), "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
     if not args.no_extra:
