@@ -177,29 +177,60 @@ def time_steps(prob, steps, warmup, flush, with_kernel_events=True):
     return starts, ends, kev, argsets
 
 
-def run_timed(prob, steps, starts, ends, argsets, flush):
+def run_timed(prob, steps, starts, ends, argsets, flush, graph=None):
     for i in range(steps):
         flush.zero_()
         starts[i].record()
-        prob.run_plan()
-        prob.run_forward(argsets[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            prob.run_plan()
+            prob.run_forward(argsets[i])
         ends[i].record()
 
 
+def capture_step(prob):
+    """plan + forward captured once as a CUDA graph (the same launches with the
+    same arguments; replay removes the host's per-launch cost, which decode-
+    sized steps would otherwise wait on)."""
+    import torch
+    args = prob.fwd_args()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            prob.run_plan()
+            prob.run_forward(args)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        prob.run_plan()
+        prob.run_forward(args)
+    torch.cuda.synchronize()
+    g._moe_args = args            # keep the argument struct alive with the graph
+    return g
+
+
 def measure(prob, steps, warmup, flush, dist=None, clocks=None):
-    """The headline: `steps` timed steps with nothing recorded between the
-    launches (they overlap through programmatic dependent launch).  Then a
-    second pass of the same steps with events between the kernels for the
+    """The headline: `steps` timed replays of the step captured as a CUDA
+    graph, nothing recorded between the launches (they overlap through
+    programmatic dependent launch).  Then the same steps issued eagerly
+    through the API, and a pass with events between the kernels for the
     per-kernel breakdown (those events serialise the launches)."""
     import torch
+    graph = capture_step(prob)
     starts, ends, _, argsets = time_steps(prob, steps, warmup, flush, with_kernel_events=False)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     if clocks:
         clocks.start()
     t0 = time.perf_counter()
-    run_timed(prob, steps, starts, ends, argsets, flush)
+    run_timed(prob, steps, starts, ends, argsets, flush, graph)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     if dist is not None:
@@ -207,11 +238,16 @@ def measure(prob, steps, warmup, flush, dist=None, clocks=None):
     clk = clocks.stop() if clocks else None
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
+    run_timed(prob, steps, starts, ends, argsets, flush)
+    torch.cuda.synchronize()
+    eager_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
     kstarts, kends, kev, kargs = time_steps(prob, steps, 1, flush, with_kernel_events=True)
     run_timed(prob, steps, kstarts, kends, kargs, flush)
     torch.cuda.synchronize()
     mean = lambda i, j: statistics.mean(k[i].elapsed_time(k[j]) for k in kev)
     return {"step_ms": statistics.mean(step_ms), "step_ms_median": statistics.median(step_ms),
+            "step_ms_eager": statistics.mean(eager_ms),
             "stage_ms": mean(0, 1), "up_ms": mean(1, 2), "down_ms": mean(2, 3), "finalize_ms": mean(3, 4),
             "plan_ms": statistics.mean(s.elapsed_time(k[0]) for s, k in zip(kstarts, kev)),
             "forward_ms": mean(0, 4), "step_ms_with_kernel_events": statistics.mean(
@@ -419,7 +455,8 @@ def run_ours(args, rank, world, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "step": "moe_plan + moe_fp8_block_scale_forward",
+        "config": {"workload": workload_desc(cfg),
+                   "step": "moe_plan + moe_fp8_block_scale_forward, captured once as a CUDA graph and replayed",
                    "l2": "flushed between steps (2 x L2 write), per-step CUDA events",
                    "parallelism": f"replicas x{world} (tokens independent, no collective)"},
         "roofline": roof,
@@ -427,6 +464,7 @@ def run_ours(args, rank, world, dist):
         "ms_kernels": {"stage": res["stage_ms"], "up": res["up_ms"], "down": res["down_ms"],
                        "finalize": res["finalize_ms"]},
         "ms_step_with_kernel_events": res["step_ms_with_kernel_events"],
+        "ms_step_eager": res["step_ms_eager"],
         "tflops_forward": w["total"]["flop"] / (res["forward_ms"] * 1e-3) / 1e12,
         "roofline_step": {"t_flop_us": w["total"]["flop"] / (fp8_peak * 1e12) * 1e6,
                           "t_bytes_us": w["total"]["bytes"] / (hbm * 1e9) * 1e6,
@@ -466,6 +504,7 @@ def extra_sweep(cfg, prob, flush, peaks):
         w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
         t_roof = max(w["total"]["flop"] / (fp8_peak * 1e12), w["total"]["bytes"] / (hbm * 1e9))
         out[name] = {"ms_step": r["step_ms"], "ms_forward": r["forward_ms"], "ms_plan": r["plan_ms"],
+                     "ms_step_eager": r["step_ms_eager"],
                      "tflops_step": w["total"]["flop"] / (r["step_ms"] * 1e-3) / 1e12,
                      "frac_roofline_step": t_roof / (r["step_ms"] * 1e-3),
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
@@ -480,8 +519,8 @@ def extra_sweep(cfg, prob, flush, peaks):
         w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
         gbs = w["total"]["bytes"] / (r["forward_ms"] * 1e-3) / 1e9
         gbs_step = w["total"]["bytes"] / (r["step_ms"] * 1e-3) / 1e9
-        out[name] = {"ms_step": r["step_ms"], "ms_forward": r["forward_ms"], "ms_plan": r["plan_ms"],
-                     "gbs_forward": gbs, "frac_hbm_forward": gbs / hbm, "gbs_step": gbs_step,
+        out[name] = {"ms_step": r["step_ms"], "ms_step_eager": r["step_ms_eager"], "ms_forward": r["forward_ms"],
+                     "ms_plan": r["plan_ms"], "gbs_forward": gbs, "frac_hbm_forward": gbs / hbm, "gbs_step": gbs_step,
                      "frac_hbm_step": gbs_step / hbm,
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
                                     "finalize": r["finalize_ms"]}}

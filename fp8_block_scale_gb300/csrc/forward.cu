@@ -136,7 +136,8 @@ struct GemmParams {
   int H;
   int a_gather4;               // up only: 1 = activation rows fetched by token with tile::gather4,
                                //          0 = rows already in plan order (2D boxes by plan slot)
-  int block_major;             // tile order: 1 = all n tiles of a plan block together, 0 = n-tile major
+  int tile_group;              // tile order: 0 = all n tiles of a plan block together (block major);
+                               // G > 0 = groups of G n tiles, within a group block major
   int splits;                  // up only: K splits per tile (1 = none)
   int ksplit;                  // K slices per split
   float* usum;                 // up, splits > 1: [nblocks, ntiles_n, block_m, 256] zeroed partial sums
@@ -170,12 +171,14 @@ __device__ __forceinline__ bool tile_coords(const GemmParams& p, const SmemCtl* 
                                             int& b, int& t, int& sp, int& e) {
   sp = static_cast<int>(tile % p.splits);
   const int64_t bt = tile / p.splits;
-  if (p.block_major) {
+  if (p.tile_group == 0) {
     b = static_cast<int>(bt / p.ntiles_n);
     t = static_cast<int>(bt % p.ntiles_n);
   } else {
-    b = static_cast<int>(bt % p.nblocks);
-    t = static_cast<int>(bt / p.nblocks);
+    const int64_t per_group = p.nblocks * p.tile_group;
+    const int64_t g = bt / per_group, r = bt - g * per_group;
+    b = static_cast<int>(r / p.tile_group);
+    t = static_cast<int>(g * p.tile_group + r % p.tile_group);
   }
   if (b >= nvalid) return false;
   if (kPair && !(ctl->pairf[b] & 1)) return false;
@@ -768,41 +771,47 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
     if (!route) continue;
     for (int k = lane; k < nkb; k += 32) p.as_t[k * p.cap_pad + slot] = __ldg(p.a_scale + tok * nkb + k);
     if (p.a_sorted) {
+      // up to 4 KB of the row in flight per warp (8 loads per lane) before the stores
       const uint4* src = reinterpret_cast<const uint4*>(p.a + tok * p.H);
       uint4* dst = reinterpret_cast<uint4*>(p.a_sorted + slot * p.H);
-      int c = lane;
-      for (; c + 96 < chunks; c += 128) {
-        const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64), v3 = __ldg(src + c + 96);
-        dst[c] = v0;
-        dst[c + 32] = v1;
-        dst[c + 64] = v2;
-        dst[c + 96] = v3;
+      for (int c0 = 0; c0 < chunks; c0 += 256) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + 32 * j + lane;
+          if (c < chunks) v[j] = __ldg(src + c);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + 32 * j + lane;
+          if (c < chunks) dst[c] = v[j];
+        }
       }
-      for (; c < chunks; c += 32) dst[c] = __ldg(src + c);
     }
   }
-  // weight-scale records
+  // weight-scale records: a CTA per plan block, its threads over the block's
+  // records (no 64-bit divisions)
   const int up_items = nib * nkb;          // (n tile: I/128 of them) x (K slice)
   const int nh = (p.H + 255) / 256;
   const int dn_items = nh * nib;
   const int per_block = up_items + dn_items;
   const int nrb13 = 2 * p.I / 128, nrb2 = p.H / 128;
-  for (int64_t i = gtid; i < nvalid * per_block; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t b = i / per_block;
-    const int j = static_cast<int>(i - b * per_block);
+  for (int64_t b = blockIdx.x; b < nvalid; b += gridDim.x) {
     const int e = p.expert_ids[b];
     if (e < 0 || e >= p.E) continue;
-    if (j < up_items) {
-      const int t = j / nkb, kb = j % nkb;
-      const float* base = p.w13_scale + static_cast<int64_t>(e) * nrb13 * nkb;
-      p.wsu[b * up_items + j] = make_float4(base[t * nkb + kb], base[(nib + t) * nkb + kb], 0.f, 0.f);
-    } else {
-      const int jj = j - up_items;
-      const int h = jj / nib, ib = jj % nib;
-      const float* base = p.w2_scale + static_cast<int64_t>(e) * nrb2 * nib;
-      const float lo = base[(2 * h) * nib + ib];
-      const float hi = (2 * h + 1 < nrb2) ? base[(2 * h + 1) * nib + ib] : 0.f;
-      p.wsd[b * dn_items + jj] = make_float4(lo, hi, 0.f, 0.f);
+    for (int j = threadIdx.x; j < per_block; j += blockDim.x) {
+      if (j < up_items) {
+        const int t = j / nkb, kb = j % nkb;
+        const float* base = p.w13_scale + static_cast<int64_t>(e) * nrb13 * nkb;
+        p.wsu[b * up_items + j] = make_float4(base[t * nkb + kb], base[(nib + t) * nkb + kb], 0.f, 0.f);
+      } else {
+        const int jj = j - up_items;
+        const int h = jj / nib, ib = jj % nib;
+        const float* base = p.w2_scale + static_cast<int64_t>(e) * nrb2 * nib;
+        const float lo = base[(2 * h) * nib + ib];
+        const float hi = (2 * h + 1 < nrb2) ? base[(2 * h + 1) * nib + ib] : 0.f;
+        p.wsd[b * dn_items + jj] = make_float4(lo, hi, 0.f, 0.f);
+      }
     }
   }
 }
@@ -1126,7 +1135,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     up.ntiles_n = N / kTileN;
     up.b_rows = N;
     up.a_gather4 = wl.pregather ? 0 : 1;
-    up.block_major = 1;
+    up.tile_group = 0;
     up.slot_tok = slot_tok;
     up.slot_w = slot_w;
     // split K when the tiles cannot fill the GPU (decode): each split streams
@@ -1167,7 +1176,17 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     dn.ntiles_n = static_cast<int>(ceil_div(a->H, kTileN));
     dn.b_rows = a->H;
     dn.a_gather4 = 0;
-    dn.block_major = 0;
+    // Groups of up to 4 n tiles: a plan block's intermediate rows are read by
+    // adjacent tiles (one DRAM read per group rather than per n tile: with a
+    // single n tile per pass, the pass's weight stream evicts them), while the
+    // route reductions of a group touch only its few 256-column stripes of
+    // the accumulator, which stay in L2.
+    dn.tile_group = 1;
+    for (int g = 4; g > 1; --g)
+      if (dn.ntiles_n % g == 0) {
+        dn.tile_group = g;
+        break;
+      }
     dn.splits = 1;
     dn.ksplit = dn.nkb;
     const int64_t dn_tiles = nblocks * dn.ntiles_n;

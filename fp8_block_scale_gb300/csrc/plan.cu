@@ -101,7 +101,9 @@ __device__ void fill_pads(int E, int block_m, int64_t R, const int* totals, cons
                           int32_t* expert_ids) {
   const int lane = threadIdx.x % 32;
   for (int e = threadIdx.x / 32; e < E; e += blockDim.x / 32) {
-    const int st = seg[e], tot = totals[e];
+    const int tot = totals[e];
+    if (tot == 0) continue;  // no routes: no slots, no blocks
+    const int st = seg[e];
     const int end = st + (tot + block_m - 1) / block_m * block_m;
     for (int q = st + tot + lane; q < end; q += 32) sorted_ids[q] = static_cast<int32_t>(R);
     for (int b = st / block_m + lane; b < end / block_m; b += 32) expert_ids[b] = e;
@@ -125,13 +127,15 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
     int carry[2] = {0, 0};
     for (int c0 = 0; c0 < nchunks; c0 += 32 * kScanBatch) {
       int v[2][kScanBatch];
+      // batches of this round that hold chunks (warp-uniform)
+      const int nbat = min(kScanBatch, (nchunks - c0 + 31) / 32);
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int32_t* row = ws.counts + static_cast<int64_t>(ee[x] < E ? ee[x] : 0) * nchunks;
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
           const int c = c0 + 32 * j + lane;
-          v[x][j] = (ee[x] < E && c < nchunks) ? row[c] : 0;
+          v[x][j] = (j < nbat && ee[x] < E && c < nchunks) ? row[c] : 0;
         }
       }
 #pragma unroll
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
         int32_t* row = ws.counts + static_cast<int64_t>(ee[x]) * nchunks;
 #pragma unroll
         for (int j = 0; j < kScanBatch; ++j) {
+          if (j >= nbat) break;
           const int c = c0 + 32 * j + lane;
           int inc = v[x][j];
 #pragma unroll

@@ -188,6 +188,30 @@ def test_forward_accumulates_and_reuses_its_workspace():
     assert rel < 2e-2, rel.item()
 
 
+@pytest.mark.parametrize("name", ["ragged_bm64", "ragged_bm128"])
+def test_plan_and_forward_replay_from_a_cuda_graph(name):
+    """Every call the library makes while launching is legal under stream
+    capture: plan + forward captured once and replayed give the oracle's
+    result (split K on the first case, plan-ordered rows on the second)."""
+    prob = DeviceProblem(SMALL[name])
+    _run(prob, debug=False)                      # first calls set the kernels' attributes
+    torch.cuda.synchronize()
+    prob.out.copy_(prob.out_prior)
+    args = prob.fwd_args()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            prob.run_plan()
+            prob.run_forward(args)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    _check(prob, np.arange(prob.cfg.M), label="graph")
+    assert int(prob.status.item()) == 0
+
+
 def test_forward_all_masked_leaves_out_unchanged():
     cfg = SMALL["tiny"].with_(name="all_masked", masked_frac=1.0)
     prob = DeviceProblem(cfg)
