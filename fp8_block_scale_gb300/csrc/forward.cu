@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tmem_relinquish_k<kPair>();
   }
   pdl_launch_dependents();
-  pdl_wait();
+  // The plan is an input of the forward, complete before its first launch
+  // began, so it is read before the dependency wait; everything the
+  // previous kernels of this forward write is read after it.
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
@@ -338,6 +340,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   const int64_t total = p.nblocks * p.ntiles_n * p.splits;
+  // the producer of a single CTA waits after prefetching weights
+  if (kPair || warp != 0) pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -346,6 +350,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     int64_t tile = MOE_CTA_ID;
     int b = 0, t = 0, sp = 0, e = 0;
     while (tile < total && !tile_coords<kPair>(p, ctl, tile, nvalid, b, t, sp, e)) tile += MOE_CTA_COUNT;
+    // Weight tiles of the first ring stages go out before the dependency
+    // wait (weights are inputs): their latency overlaps the previous
+    // kernel's tail.  Their bytes are added to the stage's transaction count
+    // without arriving, so the stage completes only after the arrival below,
+    // which also expects the activation rows and side data.
+    uint32_t npre = 0;
+    if (!kPair) {
+      int64_t pt = tile;
+      int pb = b, pt_n = t, psp = sp, pe = e;
+      int pkb = psp * p.ksplit, pkb1 = min(p.nkb, pkb + p.ksplit);
+      while (pt < total && npre < static_cast<uint32_t>(kStages)) {
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&ctl->full[npre]);
+          mbar_expect_tx(full, kBStage);
+          tma_load_2d(smem_u32(sB + npre * kBStage), &tmB, full, pkb * kTileK, pe * p.b_rows + pt_n * kTileN);
+        }
+        ++npre;
+        if (++pkb >= pkb1) {
+          pt += MOE_CTA_COUNT;
+          while (pt < total && !tile_coords<kPair>(p, ctl, pt, nvalid, pb, pt_n, psp, pe)) pt += MOE_CTA_COUNT;
+          pkb = psp * p.ksplit;
+          pkb1 = min(p.nkb, pkb + p.ksplit);
+        }
+      }
+      pdl_wait();
+    }
     // gather4 path: a tile's plan entries are read one tile ahead
     int ids[4] = {-1, -1, -1, -1};
     if (kUp && !kPair && p.a_gather4 && tile < total) load_ids(p, b, lane, ids);
@@ -375,6 +405,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       // the leader's barrier counts the operand bytes of both CTAs
       const uint32_t op_bytes = kPair ? (kABytes + (partner ? kABytes : 0u) + 2u * kBStage) : a_bytes + kBStage;
+      const uint32_t op_bytes_pre = a_bytes;  // weight tile already expected and in flight
       const int brow = e * p.b_rows + t * kTileN + static_cast<int>(rank) * kBStage / kTileK;
       const int64_t slot0 = static_cast<int64_t>(mb) * p.block_m;
       const int kb0 = sp * p.ksplit;
@@ -390,8 +421,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint32_t xfull = smem_u32(&ctl->xfull[s]);
         const bool tile_info = (!kUp || (!kPair && p.splits > 1)) && kb == kb0;
         const uint32_t extra = 512u + 16u + (tile_info ? 1024u : 0u);
+        const bool pre = it < npre;
         if (lane == 0) {
-          if (!kPair || rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), op_bytes);
+          if (!kPair || rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[s]), pre ? op_bytes_pre : op_bytes);
           mbar_arrive_expect_tx(xfull, extra);
         }
         // the small side copies go first: queued behind the operand boxes
@@ -416,7 +448,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           else
             tma_load_2d(a_dst, &tmA, full, kb * kTileK, mb * p.block_m);
         }
-        if (lane == 0) {
+        if (lane == 0 && !pre) {
           if (kPair)
             tma_load_2d_pair(smem_u32(sB + s * kBStage), &tmB, full, kb * kTileK, brow);
           else
