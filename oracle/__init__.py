@@ -27,6 +27,8 @@ Modules:
   forward pass (FP32 emulation) and an FP64 twin used to pin it.
 * ``inputs`` -- oracle-side inputs regenerated from the seeded workload
   generator, and the parity metrics (tolerances of the forward).
+* ``router`` -- top-k expert selection and route weights from router logits
+  (the reading of the companion router the pages name).
 
 Pinning status: every function here is pinned by a CPU test under
 ``tests/`` (exhaustive codec checks, closed forms, brute force on tiny inputs,
