@@ -525,8 +525,37 @@ def extra_sweep(cfg, prob, flush, peaks):
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
                                     "finalize": r["finalize_ms"]}}
     del base
+    for label, (M, E, k) in (("router_m1", (1, 257, 9)), ("router_m8192", (8192, 288, 8))):
+        out[label] = measure_router(M, E, k, flush, peaks)
     torch.cuda.empty_cache()
     return out
+
+
+def measure_router(M, E, k, flush, peaks, steps=20, warmup=5):
+    """moe_route_topk on FP32 logits (seeded normal), L2 flushed before each
+    timed call; bytes = logits read + ids and weights written."""
+    import torch
+    from fp8_block_scale_gb300 import _lib as L
+    g = torch.Generator(device="cpu").manual_seed(M * 131 + E)
+    logits = torch.randn((M, E), generator=g).cuda()
+    ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        L.moe_route_topk(logits, k, ids, w)
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        L.moe_route_topk(logits, k, ids, w)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nbytes = M * E * 4 + M * k * 8
+    return {"M": M, "E": E, "top_k": k, "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
 
 def main():

@@ -79,6 +79,9 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p]),
     "moe_requant_scales_ue8m0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_void_p]),
     "moe_quantize_act_1x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]),
     "moe_quantize_weight_128x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -155,6 +158,19 @@ def moe_requant_scales_ue8m0(w, scale, ue8m0_exp=None, stream=None):
     E, rows, cols = w.shape
     _check("moe_requant_scales_ue8m0", load().moe_requant_scales_ue8m0(
         _ptr(w), _ptr(scale), _ptr(ue8m0_exp), E, rows, cols, _stream(stream)))
+
+
+LOGITS_F32, LOGITS_BF16 = 0, 1
+
+
+def moe_route_topk(logits, top_k, topk_ids, topk_weights, routed_scale=1.0, renormalize=True, stream=None):
+    """logits [M, E] float32 or bfloat16 -> topk_ids [M, top_k] (int32/int64), topk_weights [M, top_k] f32."""
+    M, E = logits.shape
+    dtype = {torch.float32: LOGITS_F32, torch.bfloat16: LOGITS_BF16}[logits.dtype]
+    bits = {torch.int32: 32, torch.int64: 64}[topk_ids.dtype]
+    _check("moe_route_topk", load().moe_route_topk(
+        _ptr(logits), dtype, M, E, top_k, float(routed_scale), 1 if renormalize else 0, _ptr(topk_ids), bits,
+        _ptr(topk_weights), _stream(stream)))
 
 
 def moe_quantize_act_1x128(x_bf16, q, scale, stream=None):

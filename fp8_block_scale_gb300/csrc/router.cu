@@ -1,0 +1,143 @@
+// moe_route_topk: router logits -> top-k expert ids and route weights, the
+// companion step before the routing plan (FlashInfer PR #4287 description,
+// "Related Issues": companion router; the serving traces run
+// kernel_alpha_moe_fused_router ahead of the expert kernel).  The pages give
+// no formula; the reading implemented here (and in the oracle) is:
+//   ids     = the top_k largest logits of the token, equal logits by
+//             ascending expert index, listed in that order;
+//   weights = exp(l_j - m) / D, m = the token's largest logit,
+//             D = sum over the selection (renormalize) or over all E experts,
+//             times routed_scale.
+//
+// One warp per token.  Lane l holds the logits of experts l, l+32, ... in
+// registers; each of the top_k rounds takes a lane-local best untaken
+// (value, index) and a warp argmax over (value descending, index ascending),
+// so the selection compares input values only and is exact.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteMaxE = 2048;
+constexpr int kRouteMaxTopK = 32;
+constexpr int kRouteWarps = 8;
+
+__device__ __forceinline__ float load_logit(const void* logits, int dtype, int64_t i) {
+  if (dtype == 0) return static_cast<const float*>(logits)[i];
+  const uint32_t bits = static_cast<const uint16_t*>(logits)[i];
+  return __uint_as_float(bits << 16);  // BF16 -> FP32 is exact
+}
+
+template <int kPer>  // logits per lane: E <= 32 * kPer
+__global__ void __launch_bounds__(32 * kRouteWarps) route_topk_kernel(const void* logits, int dtype, int64_t M,
+                                                                      int E, int top_k, float routed_scale,
+                                                                      int renormalize, void* ids, int id_bits,
+                                                                      float* weights) {
+  const int lane = threadIdx.x % 32;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + threadIdx.x / 32;
+  if (t >= M) return;  // whole warp
+  float v[kPer];
+  uint64_t taken = 0;  // bit i: expert lane + 32 i already selected, or past E
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? load_logit(logits, dtype, t * E + e) : 0.f;
+    if (e >= E) taken |= uint64_t(1) << i;
+  }
+  constexpr int kNone = 0x7fffffff;
+  float my_l = 0.f;  // lane j < top_k: logit and expert of the j-th selection
+  int my_id = 0;
+  for (int j = 0; j < top_k; ++j) {
+    float bv = 0.f;
+    int bi = kNone;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && (bi == kNone || v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == (bi & 31)) taken |= uint64_t(1) << (bi >> 5);
+    if (lane == j) {
+      my_l = bv;
+      my_id = bi;
+    }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_l, 0);  // the largest logit
+  const float num = lane < top_k ? expf(my_l - m) : 0.f;
+  float part = num;
+  if (!renormalize) {
+    part = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i < E) part += expf(v[i] - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane < top_k) {
+    const int64_t o = t * top_k + lane;
+    weights[o] = num / part * routed_scale;
+    if (id_bits == 64)
+      static_cast<int64_t*>(ids)[o] = my_id;
+    else
+      static_cast<int32_t*>(ids)[o] = my_id;
+  }
+}
+
+template <int kPer>
+cudaError_t launch_route(const void* logits, int dtype, int64_t M, int E, int top_k, float routed_scale,
+                         int renormalize, void* ids, int id_bits, float* weights, cudaStream_t stream) {
+  const int64_t grid = ceil_div(M, static_cast<int64_t>(kRouteWarps));
+  route_topk_kernel<kPer><<<static_cast<unsigned>(grid), 32 * kRouteWarps, 0, stream>>>(
+      logits, dtype, M, E, top_k, routed_scale, renormalize, ids, id_bits, weights);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_route_topk(const void* logits, int logit_dtype, int64_t M, int E, int top_k, float routed_scale,
+                          int renormalize, void* topk_ids, int id_bits, float* topk_weights, moe_stream_t stream) {
+  using namespace moe;
+  if (logit_dtype != MOE_LOGITS_F32 && logit_dtype != MOE_LOGITS_BF16) return MOE_ERR_DTYPE;
+  if (id_bits != 32 && id_bits != 64) return MOE_ERR_DTYPE;
+  if (M < 0 || E < 1 || E > kRouteMaxE || top_k < 1 || top_k > kRouteMaxTopK || top_k > E) return MOE_ERR_SHAPE;
+  if (M * static_cast<int64_t>(E) >= (int64_t(1) << 40)) return MOE_ERR_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_weights) return MOE_ERR_NULL;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if (!on_device(logits, dev.device) || !on_device(topk_ids, dev.device) || !on_device(topk_weights, dev.device))
+    return MOE_ERR_DEVICE;
+  cudaError_t err;
+  const int per = static_cast<int>(ceil_div(static_cast<int64_t>(E), int64_t(32)));
+  if (per <= 1)
+    err = launch_route<1>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else if (per <= 2)
+    err = launch_route<2>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else if (per <= 4)
+    err = launch_route<4>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else if (per <= 8)
+    err = launch_route<8>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else if (per <= 16)
+    err = launch_route<16>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else if (per <= 32)
+    err = launch_route<32>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  else
+    err = launch_route<64>(logits, logit_dtype, M, E, top_k, routed_scale, renormalize, topk_ids, id_bits, topk_weights, stream);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

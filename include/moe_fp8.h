@@ -138,6 +138,32 @@ moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, i
                                        uint8_t* q, float* scale, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Router (the step before the plan: PR #4287 description, "Related Issues",
+ * companion router; the serving traces run the router kernel ahead of the
+ * expert kernel).  The pages give no formula; this is the reading:
+ *   ids[t, :]     = the top_k largest logits[t, :], equal logits by
+ *                   ascending expert index, in that order (exact: only input
+ *                   values are compared);
+ *   weights[t, j] = exp(l_j - m) / D * routed_scale, m = max_e logits[t, e],
+ *                   D = sum of exp(l_i - m) over the selection (renormalize
+ *                   != 0) or over all E experts (renormalize == 0).
+ * FP32 arithmetic (expf, IEEE division).  Logits must not be NaN (the
+ * selection is then unspecified; nothing is written out of bounds).
+ * ------------------------------------------------------------------------ */
+
+#define MOE_LOGITS_F32 0
+#define MOE_LOGITS_BF16 1
+
+/* logits [M, E] (MOE_LOGITS_F32: float; MOE_LOGITS_BF16: BF16 bits),
+ * row-major, device memory -> topk_ids [M, top_k] (int32 or int64 per
+ * id_bits, ready for moe_plan) and topk_weights [M, top_k] FP32, both
+ * caller-owned device memory, fully written for every token.
+ * 1 <= E <= 2048, 1 <= top_k <= min(E, 32).  Errors: MOE_ERR_DTYPE (dtype,
+ * id_bits), MOE_ERR_SHAPE, MOE_ERR_NULL, MOE_ERR_DEVICE; M == 0 is a no-op. */
+moe_status moe_route_topk(const void* logits, int logit_dtype, int64_t M, int E, int top_k, float routed_scale,
+                          int renormalize, void* topk_ids, int id_bits, float* topk_weights, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The fused forward (PR #4287 commit summary and "Public contract and review
  * fixes"; post-dot scale application, "Final W8 kernel performance (v46)").
  *

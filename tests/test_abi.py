@@ -122,3 +122,20 @@ def test_plan_and_prep_host_validation_without_gpu(lib):
     assert lib.moe_requant_scales_ue8m0(p, p, None, 1, 100, 128, None) == 2
     assert lib.moe_quantize_act_1x128(p, 4, 100, p, p, None) == 2
     assert lib.moe_quantize_weight_128x128(p, 1, 128, 64, p, p, None) == 2
+
+
+def test_router_host_validation_without_gpu(lib):
+    """moe_route_topk rejects bad arguments on the host, before any device call."""
+    f = lib.moe_route_topk
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    p = ctypes.c_void_p(4096)
+    assert f(p, 2, 4, 8, 2, 1.0, 1, p, 32, p, None) == 5          # unknown logit dtype
+    assert f(p, 0, 4, 8, 2, 1.0, 1, p, 16, p, None) == 5          # id width
+    assert f(p, 0, 4, 8, 9, 1.0, 1, p, 32, p, None) == 2          # top_k > E
+    assert f(p, 0, 4, 64, 33, 1.0, 1, p, 32, p, None) == 2        # top_k > 32
+    assert f(p, 0, 4, 2049, 2, 1.0, 1, p, 32, p, None) == 2       # E too large
+    assert f(p, 0, -1, 8, 2, 1.0, 1, p, 32, p, None) == 2         # negative M
+    assert f(None, 0, 4, 8, 2, 1.0, 1, p, 32, p, None) == 1       # null logits
+    assert f(None, 0, 0, 8, 2, 1.0, 1, None, 32, None, None) == 0  # nothing to do
