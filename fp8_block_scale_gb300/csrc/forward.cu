@@ -771,8 +771,11 @@ struct StageParams {
 };
 
 __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
-  pdl_launch_dependents();
+  // Trigger only after the wait: the GEMMs read the plan before their own
+  // dependency wait, which is sound once this grid has waited for the
+  // (programmatically launched) plan kernels.
   pdl_wait();
+  pdl_launch_dependents();
   // Clear the route accumulator for this forward's down kernel (which starts
   // after this grid completes).  Only after the wait: the previous forward's
   // finalize may still be reading it.
@@ -945,31 +948,6 @@ WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64
   return l;
 }
 
-// Launch with programmatic stream serialization (the kernel calls
-// pdl_wait), optionally as clusters of `cluster` CTAs.
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  int n = 1;
-  if (cluster > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    n = 2;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
 
 // Clusters of two CTAs that the GPU holds at once.  GPCs need not have an
 // even number of SMs, so this can be below SMs / 2; a persistent grid larger

@@ -39,8 +39,18 @@ __device__ __forceinline__ int load_id(const void* ids, int id_bits, int64_t r, 
   return (v >= 0 && v < E) ? static_cast<int>(v) : -1;
 }
 
+// Every plan kernel is launched with programmatic stream serialization: it
+// waits for its predecessor (which may have produced the ids, or may still
+// read the previous plan) before touching memory, then lets its own
+// dependents begin launching.
+__device__ __forceinline__ void plan_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
 __global__ void __launch_bounds__(kChunk) plan_rank_kernel(const void* ids, int id_bits, int64_t R, int E, PlanWs ws) {
   extern __shared__ int32_t wh[];  // [kChunkWarps][E]
+  plan_enter();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int i = threadIdx.x; i < kChunkWarps * E; i += blockDim.x) wh[i] = 0;
   __syncthreads();
@@ -116,6 +126,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
   __shared__ int scan_smem[33];
   __shared__ int totals[kMaxExperts];
   __shared__ int seg[kMaxExperts];
+  plan_enter();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   // 1. one warp per expert: exclusive scan of its chunk counts (bases inside
   //    the expert) and the expert's total.  A warp takes two experts at a
@@ -193,6 +204,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
 
 __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, int id_bits, int64_t R, int E, PlanWs ws,
                                                                int32_t* sorted_ids) {
+  plan_enter();
   const int64_t r = static_cast<int64_t>(blockIdx.x) * kChunk + threadIdx.x;
   if (r >= R) return;
   const int rk = ws.rank[r];
@@ -214,6 +226,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* id
   __shared__ int totals[kSmallMaxExperts];
   __shared__ int seg[kSmallMaxExperts];
   constexpr int kWarps = kScanThreads / 32;
+  plan_enter();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wh[i] = 0;
   __syncthreads();
@@ -319,24 +332,21 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
   }
   if (R <= kSmallRoutes && E <= kSmallMaxExperts) {
     const size_t small_smem = static_cast<size_t>(kScanThreads / 32) * E * sizeof(int32_t);
-    plan_small_kernel<<<1, kScanThreads, small_smem, stream>>>(topk_ids, id_bits, R, E, block_m, sorted_token_ids,
-                                                                expert_ids, num_tokens_post_padded);
-    MOE_CUDA_TRY(cudaGetLastError());
+    MOE_CUDA_TRY(launch_pdl(plan_small_kernel, dim3(1), dim3(kScanThreads), small_smem, stream, 1, topk_ids, id_bits,
+                            R, E, block_m, sorted_token_ids, expert_ids, num_tokens_post_padded));
     return MOE_OK;
   }
   if (R > 0) {
-    plan_rank_kernel<<<static_cast<unsigned>(nchunks), kChunk, smem, stream>>>(topk_ids, id_bits, R, E, ws);
-    MOE_CUDA_TRY(cudaGetLastError());
+    MOE_CUDA_TRY(launch_pdl(plan_rank_kernel, dim3(static_cast<unsigned>(nchunks)), dim3(kChunk), smem, stream, 1,
+                            topk_ids, id_bits, R, E, ws));
   } else {
     nchunks = 0;
   }
-  plan_scan_kernel<<<1, kScanThreads, 0, stream>>>(R, E, block_m, static_cast<int>(nchunks), ws, sorted_token_ids,
-                                                   expert_ids, num_tokens_post_padded);
-  MOE_CUDA_TRY(cudaGetLastError());
+  MOE_CUDA_TRY(launch_pdl(plan_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, 1, R, E, block_m,
+                          static_cast<int>(nchunks), ws, sorted_token_ids, expert_ids, num_tokens_post_padded));
   if (R > 0) {
-    plan_scatter_kernel<<<static_cast<unsigned>(nchunks), kChunk, 0, stream>>>(topk_ids, id_bits, R, E, ws,
-                                                                               sorted_token_ids);
-    MOE_CUDA_TRY(cudaGetLastError());
+    MOE_CUDA_TRY(launch_pdl(plan_scatter_kernel, dim3(static_cast<unsigned>(nchunks)), dim3(kChunk), 0, stream, 1,
+                            topk_ids, id_bits, R, E, ws, sorted_token_ids));
   }
   return MOE_OK;
 }

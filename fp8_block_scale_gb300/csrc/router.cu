@@ -33,6 +33,11 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_topk_kernel(const void
                                                                       int E, int top_k, float routed_scale,
                                                                       int renormalize, void* ids, int id_bits,
                                                                       float* weights) {
+  // launched with programmatic stream serialization: wait for the
+  // predecessor (it may still read the previous ids), then release the
+  // dependents (the plan waits for this grid in turn)
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + threadIdx.x / 32;
   if (t >= M) return;  // whole warp
@@ -98,9 +103,8 @@ template <int kPer>
 cudaError_t launch_route(const void* logits, int dtype, int64_t M, int E, int top_k, float routed_scale,
                          int renormalize, void* ids, int id_bits, float* weights, cudaStream_t stream) {
   const int64_t grid = ceil_div(M, static_cast<int64_t>(kRouteWarps));
-  route_topk_kernel<kPer><<<static_cast<unsigned>(grid), 32 * kRouteWarps, 0, stream>>>(
-      logits, dtype, M, E, top_k, routed_scale, renormalize, ids, id_bits, weights);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel<kPer>, dim3(static_cast<unsigned>(grid)), dim3(32 * kRouteWarps), 0, stream, 1,
+                    logits, dtype, M, E, top_k, routed_scale, renormalize, ids, id_bits, weights);
 }
 
 }  // namespace
