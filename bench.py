@@ -3,8 +3,9 @@
 
 One step = one pass of the hot path over one batch: the routing plan
 (moe_plan) and the fused forward (moe_fp8_block_scale_forward: gate/up GEMM +
-SwiGLU + requant, down GEMM + route reduce, BF16 finalize), on the prefill
-workload E288/H4096/I1024/top-8 at 8192 tokens, inputs resident in HBM.
+SwiGLU + requant, down GEMM writing BF16 route contributions, combine onto
+out), on the prefill workload E288/H4096/I1024/top-8 at 8192 tokens, inputs
+resident in HBM.
 L2 is flushed (a write larger than L2) between timed steps, outside the
 timed intervals, and each step is timed with CUDA events on its stream.
 
@@ -30,7 +31,7 @@ if ROOT not in sys.path:
 METRIC = "fused FP8 MoE ms/call & TFLOPS (E288 H4096 I1024 top8, 1K-8K tok), % roofline"
 UNIT = "TFLOP/s"
 HEADLINE = "prefill_8192"
-# our kernels per step: moe_plan (rank, scan, scatter) + forward (stage, gate/up, down, finalize)
+# our kernels per step: moe_plan (rank, scan, scatter) + forward (stage, gate/up, down, combine)
 LAUNCHES_PER_STEP = 7
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -248,7 +249,7 @@ def measure(prob, steps, warmup, flush, dist=None, clocks=None):
     mean = lambda i, j: statistics.mean(k[i].elapsed_time(k[j]) for k in kev)
     return {"step_ms": statistics.mean(step_ms), "step_ms_median": statistics.median(step_ms),
             "step_ms_eager": statistics.mean(eager_ms),
-            "stage_ms": mean(0, 1), "up_ms": mean(1, 2), "down_ms": mean(2, 3), "finalize_ms": mean(3, 4),
+            "stage_ms": mean(0, 1), "up_ms": mean(1, 2), "down_ms": mean(2, 3), "combine_ms": mean(3, 4),
             "plan_ms": statistics.mean(s.elapsed_time(k[0]) for s, k in zip(kstarts, kev)),
             "forward_ms": mean(0, 4), "step_ms_with_kernel_events": statistics.mean(
                 s.elapsed_time(e) for s, e in zip(kstarts, kends)),
@@ -534,7 +535,7 @@ def run_ours(args, rank, world, dist):
         "roofline": roof,
         "ms_forward": res["forward_ms"], "ms_plan": res["plan_ms"],
         "ms_kernels": {"stage": res["stage_ms"], "up": res["up_ms"], "down": res["down_ms"],
-                       "finalize": res["finalize_ms"]},
+                       "combine": res["combine_ms"]},
         "ms_step_with_kernel_events": res["step_ms_with_kernel_events"],
         "ms_step_eager": res["step_ms_eager"],
         "tflops_forward": w["total"]["flop"] / (res["forward_ms"] * 1e-3) / 1e12,
@@ -583,7 +584,7 @@ def extra_sweep(cfg, prob, flush, peaks):
                      "tflops_step": w["total"]["flop"] / (r["step_ms"] * 1e-3) / 1e12,
                      "frac_roofline_step": t_roof / (r["step_ms"] * 1e-3),
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
-                                    "finalize": r["finalize_ms"]}}
+                                    "combine": r["combine_ms"]}}
         del p
     base = None
     for name in ("decode_m1", "decode_m8", "decode_m64"):
@@ -598,7 +599,7 @@ def extra_sweep(cfg, prob, flush, peaks):
                      "ms_plan": r["plan_ms"], "gbs_forward": gbs, "frac_hbm_forward": gbs / hbm, "gbs_step": gbs_step,
                      "frac_hbm_step": gbs_step / hbm,
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
-                                    "finalize": r["finalize_ms"]}}
+                                    "combine": r["combine_ms"]}}
     del base
     for label, (M, E, k) in (("router_m1", (1, 257, 9)), ("router_m8192", (8192, 288, 8))):
         out[label] = measure_router(M, E, k, flush, peaks)

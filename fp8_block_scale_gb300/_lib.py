@@ -223,7 +223,7 @@ def make_fwd_args(a, a_scale, w13, w13_scale, w2, w2_scale, topk_weights, sorted
     return args
 
 
-PROFILE_EVENTS = 5  # before staging, after staging, after gate/up, after down, after finalize
+PROFILE_EVENTS = 5  # before staging, after staging, after gate/up, after down, after combine
 
 
 def set_profile_events(args, events):

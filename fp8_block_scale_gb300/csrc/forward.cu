@@ -19,7 +19,7 @@
 //   2. down (gemm kernel, kUp = false): intermediate rows x W2 tile, promoted
 //      with the intermediate and W2 block scales, times the route weight and
 //      routed scale, reduced into an FP32 [M, H] accumulator.
-//   3. finalize: out = bf16_rn(f32(out) + acc); acc = 0.
+//   3. combine: out = bf16_rn(f32(out) + sum of the token's route rows).
 //
 // The GEMM kernel is persistent and warp specialised (320 threads):
 //   warp 0      TMA producer: activation (or intermediate) rows, the 256-row
@@ -68,17 +68,12 @@ template <bool kPair> struct Cfg {
 // Per-stage side data, filled by bulk copies next to the operand tiles.
 struct StageExtra {
   float a_scale[kTileM];     // activation (up) / intermediate (down) scale of each tile row
-  int32_t tok[kTileM];       // first slice of a tile: token of each row (-1 = no route)
+  int32_t tok[kTileM];       // first slice of a tile: route id of each row (-1 = no route)
   float weight[kTileM];      // down, first slice of a tile: route weight x routed scale
   float4 w_scale;            // the tile's two weight block scales for this K slice
   float4 pad0;
 };
 static_assert(sizeof(StageExtra) == 1568 && sizeof(StageExtra) % 16 == 0, "stage extra layout");
-
-// Down kernel: each epilogue warp transposes its 32 rows x 16 columns
-// through a buffer so that one vector reduction covers 8 rows x 64
-// contiguous bytes instead of 32 scattered rows.
-constexpr int kRedCols = 16;
 
 struct SmemCtl {
   uint64_t full[kMaxStages];       // operand tiles landed (the leader's counts both CTAs of a pair)
@@ -92,14 +87,14 @@ struct SmemCtl {
   int pad;
   union alignas(16) Scratch {
     float xchg[2][2][kTileM];                   // up: [tile parity][column half][row] amax exchange
-    float red[kNumEpiWarps][32][kRedCols + 4];  // down: per-warp transpose buffer (padded rows), float4 access
+    uint32_t yt[kNumEpiWarps][32][20];          // down: per-warp transpose of 32 rows x 32 BF16 (padded rows)
   } u;
   int32_t row_tok[kTileM];         // up with split K: token of each tile row (-1 = no route)
   int32_t expert[kMaxBlocksSmem];  // expert of each plan block (cached at start)
   uint8_t pairf[kMaxBlocksSmem];   // pair mode: bit 0 leads a pair, bit 1 has a partner
 };
 
-static_assert(offsetof(SmemCtl, u) % 16 == 0, "vector accesses to the transpose buffer need 16-byte alignment");
+static_assert(offsetof(SmemCtl, u) % 16 == 0, "scratch alignment");
 static_assert(sizeof(SmemCtl) % 16 == 0, "control block size");
 
 template <bool kPair>
@@ -115,9 +110,9 @@ struct GemmParams {
   const int32_t* sorted_ids;   // up with gather4: plan (token of each row)
   const float* a_scale_t;      // [nkb, cap_pad]: scale of each plan slot per K slice
   const float4* w_scale_st;    // [nblocks, ntiles_n, nkb]: weight scales per tile and slice
-  const int32_t* slot_tok;     // [cap_pad] token per plan slot (-1 = pad)
+  const int32_t* slot_route;   // [cap_pad] route id r = t * top_k + j per plan slot (-1 = pad)
   const float* slot_w;         // [cap_pad] route weight x routed scale
-  float* acc_out;              // down: [M, H]
+  uint16_t* y_out;             // down: [R, H] BF16 route contributions y * w, by route id
   uint8_t* q_inter;            // up: [sorted_cap, I]
   float* s_inter_t;            // up: [I/128, cap_pad]
   uint8_t* dbg_q;              // up, nullable: [sorted_cap, I]
@@ -142,6 +137,7 @@ struct GemmParams {
   int ksplit;                  // K slices per split
   float* usum;                 // up, splits > 1: [nblocks, ntiles_n, block_m, 256] zeroed partial sums
   int32_t* ucnt;               // up, splits > 1: [nblocks, ntiles_n] zeroed arrival tickets
+  uint32_t* gen;               // up: forward stamp, advanced once per forward
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -342,6 +338,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const int64_t total = p.nblocks * p.ntiles_n * p.splits;
   // the producer of a single CTA waits after prefetching weights
   if (kPair || warp != 0) pdl_wait();
+  // the staging kernel (complete now) stamped this forward's routes with
+  // gen + 1; the combine reads the advanced value
+  if (kUp && p.gen && blockIdx.x == 0 && threadIdx.x == 64) *p.gen += 1u;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -434,7 +433,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           bulk_load(smem_u32(&x->w_scale), p.w_scale_st + (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb, 16u,
                     xfull);
           if (tile_info) {
-            bulk_load(smem_u32(x->tok), p.slot_tok + slot0, 512u, xfull);
+            bulk_load(smem_u32(x->tok), p.slot_route + slot0, 512u, xfull);
             bulk_load(smem_u32(x->weight), p.slot_w + slot0, 512u, xfull);
           }
         }
@@ -689,38 +688,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
       } else if (!kUp) {
+        // this row's contribution y * w for its route (`tok` holds the route
+        // id), rounded to BF16: 128 columns = 256 contiguous bytes
+        // Stored transposed through shared memory, 32 columns at a time, so
+        // one instruction writes 8 rows x 64 contiguous bytes.
         const int hblk = 2 * t + half;
-        if (ok && hblk < p.H / 128) {
-          // rows of this warp: quarter*32 + r; lane l reduces row 8*i + l/4,
-          // columns 4*(l%4) .. +3 of each 16-column chunk
-          const bool live = MOE_RVALID && tok >= 0;
-          if (__any_sync(0xffffffffu, live)) {
-            float(*buf)[kRedCols + 4] = ctl->u.red[warp - 2];
-            const int sub = lane >> 2, c4 = 4 * (lane & 3);
-            int toks[4];
-            float* dst[4];
+        const bool live = ok && hblk < p.H / 128 && MOE_RVALID && tok >= 0;
+        if (__any_sync(0xffffffffu, live)) {
+          uint32_t(*buf)[20] = ctl->u.yt[warp - 2];
+          const int sub = lane >> 2, c16 = lane & 3;  // row 8 i + sub, 16-byte segment c16 of 64
+          int rts[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rts[i] = __shfl_sync(0xffffffffu, live ? tok : -1, 8 * i + sub);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const int c = 32 * ch + 2 * w;
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__fmul_rn(acc[c], wr), __fmul_rn(acc[c + 1], wr));
+              buf[lane][w] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            __syncwarp();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              toks[i] = __shfl_sync(0xffffffffu, live ? tok : -1, 8 * i + sub);
-              dst[i] = p.acc_out + static_cast<int64_t>(toks[i] < 0 ? 0 : toks[i]) * p.H + hblk * 128 + c4;
-            }
-#pragma unroll
-            for (int ch = 0; ch < 128 / kRedCols; ++ch) {
-#pragma unroll
-              for (int j = 0; j < kRedCols; j += 4)
-                *reinterpret_cast<float4*>(&buf[lane][j]) =
-                    make_float4(__fmul_rn(acc[ch * kRedCols + j], wr), __fmul_rn(acc[ch * kRedCols + j + 1], wr),
-                                __fmul_rn(acc[ch * kRedCols + j + 2], wr), __fmul_rn(acc[ch * kRedCols + j + 3], wr));
-              __syncwarp();
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (toks[i] >= 0) {
-                  const float4 v = *reinterpret_cast<const float4*>(&buf[8 * i + sub][c4]);
-                  red_add_v4(dst[i] + ch * kRedCols, v.x, v.y, v.z, v.w);
-                }
+              if (rts[i] >= 0) {
+                const uint32_t* src = &buf[8 * i + sub][4 * c16];
+                uint4* dst = reinterpret_cast<uint4*>(p.y_out + static_cast<int64_t>(rts[i]) * p.H + hblk * 128 +
+                                                      32 * ch + 8 * c16);
+                *dst = make_uint4(src[0], src[1], src[2], src[3]);
               }
-              __syncwarp();
             }
+            __syncwarp();
           }
         }
       }
@@ -758,12 +756,12 @@ struct StageParams {
   const float* w2_scale;
   uint8_t* a_sorted;          // nullable: no row copy
   float* as_t;                // [nkb, cap_pad]
-  int32_t* slot_tok;          // [cap_pad]
+  int32_t* slot_route;        // [cap_pad]
+  uint32_t* rvalid;           // [R] set to this forward's stamp for each route the plan holds
+  const uint32_t* gen;        // stamp of the previous forward (this one's is gen + 1)
   float* slot_w;              // [cap_pad]
   float4* wsu;                // [nblocks, I/128, H/128]
   float4* wsd;                // [nblocks, ceil(H/256), I/128]
-  float4* acc;                // [M * H / 4] route accumulator, zeroed here for the down kernel
-  int64_t acc_n4;
   int64_t nblocks;
   int64_t cap_pad;
   int R, top_k, block_m, E, H, I;
@@ -776,15 +774,6 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   // (programmatically launched) plan kernels.
   pdl_wait();
   pdl_launch_dependents();
-  // Clear the route accumulator for this forward's down kernel (which starts
-  // after this grid completes).  Only after the wait: the previous forward's
-  // finalize may still be reading it.
-  {
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < p.acc_n4; i += stride)
-      __stcs(p.acc + i, z);
-  }
   int64_t P = *p.num_post_padded;
   if (P < 0) P = 0;
   int64_t nvalid = P / p.block_m;
@@ -800,8 +789,9 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
     const bool route = id >= 0 && id < p.R;
     const int64_t tok = route ? id / p.top_k : 0;
     if (lane == 0) {
-      p.slot_tok[slot] = route ? static_cast<int32_t>(tok) : -1;
+      p.slot_route[slot] = route ? id : -1;
       p.slot_w[slot] = route ? __fmul_rn(__ldg(p.topk_w + id), p.routed_scale) : 0.f;
+      if (route) p.rvalid[id] = *p.gen + 1u;
     }
     if (!route) continue;
     for (int k = lane; k < nkb; k += 32) p.as_t[k * p.cap_pad + slot] = __ldg(p.a_scale + tok * nkb + k);
@@ -851,46 +841,81 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   }
 }
 
-// out = bf16_rn(f32(out) + acc).  Eight elements per thread.
-__device__ __forceinline__ uint4 add_bf16x8(uint4 o, float4 a0, float4 a1) {
-  const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+// Combine: out[t] = bf16_rn(f32(out[t]) + sum_j f32(y[t * top_k + j])) over
+// the token's routes that the plan holds (their flag carries this forward's
+// stamp), in route order.  A warp per (token, 256-column segment); a token's
+// routes are adjacent rows of y.  Rows are loaded eight routes at a time
+// whether or not the plan holds them (every row lies inside y), so the
+// first loads go out together with the flags; rows of routes not held are
+// never added.
+__device__ __forceinline__ void add_bf16x8(float (&f)[8], const uint4 v) {
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float lo = __fadd_rn(__uint_as_float((ow[k] & 0xFFFFu) << 16), av[2 * k]);
-    const float hi = __fadd_rn(__uint_as_float(ow[k] & 0xFFFF0000u), av[2 * k + 1]);
-    const uint32_t blo = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t bhi = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    ow[k] = blo | (bhi << 16);
+    f[2 * k] = __fadd_rn(f[2 * k], __uint_as_float(vw[k] << 16));
+    f[2 * k + 1] = __fadd_rn(f[2 * k + 1], __uint_as_float(vw[k] & 0xFFFF0000u));
   }
-  return o;
 }
 
-// Two groups of eight per iteration, all loads issued before any store.  The
-// accumulator is left as it is: the next forward's staging kernel clears it
-// (rewriting the lines just read here cost more than the rest of the pass).
-__global__ void __launch_bounds__(256) finalize_kernel(uint16_t* __restrict__ out, const float* __restrict__ acc,
-                                                       int64_t n8) {
-  uint4* o4 = reinterpret_cast<uint4*>(out);
-  const float4* a4 = reinterpret_cast<const float4*>(acc);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+__global__ void __launch_bounds__(256) combine_kernel(uint16_t* __restrict__ out, const uint16_t* __restrict__ y,
+                                                      const uint32_t* __restrict__ rvalid, const uint32_t* gen,
+                                                      int64_t M, int H, int top_k) {
+  constexpr int kBatch = 8;
   pdl_launch_dependents();
   pdl_wait();
-  for (; i + stride < n8; i += 2 * stride) {
-    const int64_t j = i + stride;
-    const uint4 o0 = o4[i], o1 = o4[j];
-    const float4 a0 = __ldcs(a4 + 2 * i), a1 = __ldcs(a4 + 2 * i + 1), b0 = __ldcs(a4 + 2 * j),
-                 b1 = __ldcs(a4 + 2 * j + 1);
-    o4[i] = add_bf16x8(o0, a0, a1);
-    o4[j] = add_bf16x8(o1, b0, b1);
-  }
-  if (i < n8) {
-    const uint4 o0 = o4[i];
-    const float4 a0 = __ldcs(a4 + 2 * i), a1 = __ldcs(a4 + 2 * i + 1);
-    o4[i] = add_bf16x8(o0, a0, a1);
+  const uint32_t stamp = *gen;  // this forward's stamp on the routes its plan holds
+  const int lane = threadIdx.x % 32;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  const int chunks = H / 8;             // 16-byte groups of eight BF16
+  const int segs = (chunks + 31) / 32;  // 256-column segments: a warp each
+  for (int64_t wi = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) / 32; wi < M * segs; wi += nwarps) {
+    const int64_t t = wi / segs;
+    const int seg = static_cast<int>(wi - t * segs);
+    const int c = 32 * seg + lane;
+    const bool in = c < chunks;
+    uint4* o4 = reinterpret_cast<uint4*>(out + t * H);
+    const uint4* y4 = reinterpret_cast<const uint4*>(y + t * top_k * static_cast<int64_t>(H)) + c;
+    const uint32_t* rv = rvalid + t * top_k;
+    // flags (top_k <= 64), the out chunk and the first batch of rows
+    const uint32_t fl0 = lane < top_k ? rv[lane] : 0u;
+    const uint32_t fl1 = lane + 32 < top_k ? rv[lane + 32] : 0u;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 o = in ? o4[c] : zero;
+    uint4 v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) v[j] = (in && j < top_k) ? __ldcs(y4 + static_cast<int64_t>(j) * chunks) : zero;
+    const unsigned vm0 = __ballot_sync(0xffffffffu, lane < top_k && fl0 == stamp);
+    const unsigned vm1 = __ballot_sync(0xffffffffu, lane + 32 < top_k && fl1 == stamp);
+    const unsigned long long vm = (static_cast<unsigned long long>(vm1) << 32) | vm0;
+    float f[8];
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(ow[k] << 16);
+      f[2 * k + 1] = __uint_as_float(ow[k] & 0xFFFF0000u);
+    }
+    for (int j0 = 0; j0 < top_k; j0 += kBatch) {
+      if (j0 > 0) {
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+          v[j] = (in && j0 + j < top_k) ? __ldcs(y4 + static_cast<int64_t>(j0 + j) * chunks) : zero;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if ((vm >> (j0 + j)) & 1ull) add_bf16x8(f, v[j]);
+    }
+    if (in) {
+      uint32_t r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+        r[k] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      o4[c] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
   }
 }
+
 
 // Activation rows are copied into plan order when plan blocks are well
 // filled (at least 8 routes per touched expert on average): tile::gather4
@@ -913,7 +938,7 @@ int64_t block_bound(int64_t R, int E, int block_m) {
 constexpr int64_t kSplitTileLimit = 256;
 
 struct WsLayout {
-  size_t acc_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, usum_off, ucnt_off, total;
+  size_t y_off, rv_off, gen_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, usum_off, ucnt_off, total;
   int64_t cap_pad, nblocks;
   bool pregather, splitk;
 };
@@ -932,7 +957,9 @@ WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64
     off += static_cast<size_t>(round_up(bytes, 256));
     return at;
   };
-  l.acc_off = take(M * H * 4);
+  l.y_off = take(R * H * 2);  // BF16 route contributions, by route id
+  l.rv_off = take(R * 4);     // route flags: the stamp of the last forward whose plan held the route
+  l.gen_off = take(4);        // the last forward's stamp
   l.q_off = take(sorted_cap * I);
   l.st_off = take(static_cast<int64_t>(nib) * l.cap_pad * 4);
   l.ast_off = take(static_cast<int64_t>(nkb) * l.cap_pad * 4);
@@ -1015,7 +1042,8 @@ size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t stream) {
   using namespace moe;
   if (!a) return MOE_ERR_NULL;
-  if (a->M < 0 || a->H < 128 || a->H % 128 || a->I < 128 || a->I % 128 || a->E < 1 || a->top_k < 1)
+  if (a->M < 0 || a->H < 128 || a->H % 128 || a->I < 128 || a->I % 128 || a->E < 1 || a->top_k < 1 ||
+      a->top_k > 64)
     return MOE_ERR_SHAPE;
   if (a->block_m < 8 || a->block_m > 128 || a->block_m % 8) return MOE_ERR_SHAPE;
   if (a->tile_mode != MOE_TILE_AUTO && a->tile_mode != MOE_TILE_SINGLE && a->tile_mode != MOE_TILE_PAIR)
@@ -1049,11 +1077,13 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   if (!set_smem_attrs(dev.device)) return MOE_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
-  float* acc = reinterpret_cast<float*>(ws + wl.acc_off);
+  uint16_t* yr = reinterpret_cast<uint16_t*>(ws + wl.y_off);
+  uint32_t* rvalid = reinterpret_cast<uint32_t*>(ws + wl.rv_off);
+  uint32_t* gen = reinterpret_cast<uint32_t*>(ws + wl.gen_off);
   uint8_t* q_inter = ws + wl.q_off;
   float* s_inter_t = reinterpret_cast<float*>(ws + wl.st_off);
   float* as_t = reinterpret_cast<float*>(ws + wl.ast_off);
-  int32_t* slot_tok = reinterpret_cast<int32_t*>(ws + wl.tok_off);
+  int32_t* slot_route = reinterpret_cast<int32_t*>(ws + wl.tok_off);
   float* slot_w = reinterpret_cast<float*>(ws + wl.w_off);
   float4* wsu = reinterpret_cast<float4*>(ws + wl.wsu_off);
   float4* wsd = reinterpret_cast<float4*>(ws + wl.wsd_off);
@@ -1100,12 +1130,12 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     sp.w2_scale = a->w2_scale;
     sp.a_sorted = a_sorted;
     sp.as_t = as_t;
-    sp.slot_tok = slot_tok;
+    sp.slot_route = slot_route;
+    sp.rvalid = rvalid;
+    sp.gen = gen;
     sp.slot_w = slot_w;
     sp.wsu = wsu;
     sp.wsd = wsd;
-    sp.acc = reinterpret_cast<float4*>(acc);
-    sp.acc_n4 = a->M * a->H / 4;
     sp.nblocks = nblocks;
     sp.cap_pad = wl.cap_pad;
     sp.R = static_cast<int>(R);
@@ -1146,7 +1176,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     up.b_rows = N;
     up.a_gather4 = wl.pregather ? 0 : 1;
     up.tile_group = 0;
-    up.slot_tok = slot_tok;
+    up.slot_route = slot_route;
+    up.gen = gen;
     up.slot_w = slot_w;
     // split K when the tiles cannot fill the GPU (decode): each split streams
     // a share of the weights, the last one to finish applies SwiGLU
@@ -1179,9 +1210,9 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     GemmParams dn = p;
     dn.a_scale_t = s_inter_t;
     dn.w_scale_st = wsd;
-    dn.slot_tok = slot_tok;
+    dn.slot_route = slot_route;
     dn.slot_w = slot_w;
-    dn.acc_out = acc;
+    dn.y_out = yr;
     dn.nkb = a->I / 128;
     dn.ntiles_n = static_cast<int>(ceil_div(a->H, kTileN));
     dn.b_rows = a->H;
@@ -1216,11 +1247,13 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   }
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[3], stream));
 
-  const int64_t n8 = a->M * a->H / 8;
-  int64_t fgrid = ceil_div(n8, 256);
-  if (fgrid > static_cast<int64_t>(dev.sms) * 16) fgrid = static_cast<int64_t>(dev.sms) * 16;
+  const int64_t segs = ceil_div(a->H / 8, int64_t(32));
+  int64_t fgrid = ceil_div(a->M * segs, int64_t(8));  // a warp per (token, 256-column segment)
+  if (fgrid > static_cast<int64_t>(dev.sms) * 32) fgrid = static_cast<int64_t>(dev.sms) * 32;
   MOE_CUDA_TRY(
-      launch_pdl(finalize_kernel, dim3(static_cast<unsigned>(fgrid)), dim3(256), 0, stream, 1, a->out, acc, n8));
+      launch_pdl(combine_kernel, dim3(static_cast<unsigned>(fgrid)), dim3(256), 0, stream, 1, a->out, yr,
+                 static_cast<const uint32_t*>(rvalid), static_cast<const uint32_t*>(gen), a->M, a->H, a->top_k));
+
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[4], stream));
   return MOE_OK;
 }

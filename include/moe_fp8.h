@@ -175,9 +175,12 @@ moe_status moe_route_topk(const void* logits, int logit_dtype, int64_t M, int E,
  *   q, s   = per-128-column E4M3 requant of h (scale amax/448; zero -> 0)
  *   y[c]   = sum_ib f32(dot128(q, w2[e, c])) * s[ib] * w2_scale[e, c/128, ib]
  *   out[t, c] += y[c] * topk_weights[t, j] * routed_scale
- * The route contributions are summed in FP32 and `out` is rounded to BF16
- * once per call: out = bf16_rn(f32(out) + sum).  Blocks past P exit
- * untouched; pad slots (id >= R) contribute nothing.
+ * Each route's contribution y * w is rounded to BF16 once; a token's
+ * contributions are added in route order to f32(out) in FP32 and `out` is
+ * rounded to BF16 once per call: out = bf16_rn(f32(out) + sum_j c_j).  (The
+ * pages' kernel reduce-adds every contribution into BF16 `out`, one rounding
+ * per add.)  Blocks past P exit untouched; pad slots (id >= R) and routes
+ * the plan does not hold contribute nothing.
  * ------------------------------------------------------------------------ */
 typedef struct moe_fwd_args {
   const uint8_t* a;                        /* [M, H] E4M3 activations                       */
@@ -208,7 +211,7 @@ typedef struct moe_fwd_args {
   void* const* profile_events;             /* nullable: 5 cudaEvent_t handles, recorded on
                                               `stream` before the staging kernel, after it,
                                               after the gate/up kernel, after the down kernel
-                                              and after the finalize kernel (per-kernel
+                                              and after the combine kernel (per-kernel
                                               timing; events between the launches keep them
                                               from overlapping; no effect if NULL)           */
   int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
@@ -228,7 +231,7 @@ typedef struct moe_fwd_args {
 #define MOE_TILE_PAIR 2
 
 /* Workspace bytes the forward needs (host-only; 0 for invalid sizes).  The
- * workspace holds an FP32 [M, H] route accumulator, the requantised
+ * workspace holds the BF16 route contributions [M * top_k, H], the requantised
  * intermediate (sorted_cap x I codes and sorted_cap x I/128 scales) and, for
  * well-filled plans (M * top_k >= 8 * min(E, M * top_k)), the activation rows
  * and scales copied into plan order (sorted_cap x H bytes and
@@ -237,15 +240,20 @@ size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int
                                   int64_t sorted_cap);
 
 /* Zero a forward workspace (async).  A workspace must be zeroed once before
- * its first forward; every forward leaves it ready for the next (the parts
- * that must be zero on entry are returned to zero; the FP32 route
- * accumulator, the first M * H * 4 bytes, is scratch the forward clears
- * itself and leaves holding the last call's sums).  Two
- * forwards that share a workspace must not run concurrently. */
+ * its first forward for a given set of sizes (M, H, I, E, top_k, block_m,
+ * sorted_cap); every forward with those sizes leaves it ready for the next:
+ * split-K tickets and partial sums go back to zero, and each route's flag
+ * holds the stamp of the last forward whose plan held it, against a stamp
+ * counter the gate/up kernel advances once per forward (so a replayed CUDA
+ * graph stays correct).  The layout depends on the sizes, so before a
+ * forward with other sizes zero the workspace again (or use another one).
+ * The BF16 route contributions, the first M * top_k * H * 2 bytes, are
+ * scratch written before they are read.  Two forwards that share a
+ * workspace must not run concurrently. */
 moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Run the forward.  Constraints: H % 128 == 0; I % 128 == 0 (so 2I % 256 ==
- * 0); 8 <= block_m <= 128, block_m % 8 == 0; sorted_cap >= blocks_cap *
+ * 0); 1 <= top_k <= 64; 8 <= block_m <= 128, block_m % 8 == 0; sorted_cap >= blocks_cap *
  * block_m; blocks_cap >= 1; a, w13, w2 and the workspace 16-byte aligned; all
  * pointers on the current device, which must be sm_100 class or newer. */
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t stream);

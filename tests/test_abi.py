@@ -60,11 +60,11 @@ def test_plan_capacity_matches_oracle(lib, M, k, E, bm):
 def test_workspace_sizes(lib):
     from fp8_block_scale_gb300 import moe_forward_workspace_size, moe_plan_workspace_size
     ws = moe_forward_workspace_size(8192, 4096, 1024, 288, 8, 128, 102400)
-    # accumulator + intermediate + activation rows in plan order (well-filled plan)
-    assert ws >= 8192 * 4096 * 4 + 102400 * 1024 + 102400 * 8 * 4 + 102400 * 4096
+    # BF16 route contributions + intermediate + activation rows in plan order (well-filled plan)
+    assert ws >= 8192 * 8 * 4096 * 2 + 102400 * 1024 + 102400 * 8 * 4 + 102400 * 4096
     # a decode-sized plan keeps the activations where they are
     small = moe_forward_workspace_size(8, 7168, 256, 257, 9, 64, 4608)
-    assert 8 * 7168 * 4 + 4608 * 256 <= small < 8 * 7168 * 4 + 4608 * 256 + 4608 * 7168
+    assert 72 * 7168 * 2 + 4608 * 256 <= small < 72 * 7168 * 2 + 4608 * 256 + 4608 * 7168
     assert moe_forward_workspace_size(8, 7168, 256, 0, 9, 64, 4608) == 0
     assert moe_plan_workspace_size(8192, 8, 288) >= 8192 * 8 * 4 + 288 * 4
 

@@ -169,16 +169,16 @@ def test_forward_modes_agree():
 # ------------------------------------------------------------------ semantics
 
 def test_forward_accumulates_and_reuses_its_workspace():
-    """out accumulates across calls; the route accumulator at the start of the
-    workspace is scratch the forward clears itself (here it holds huge values
-    before the second call), and the split-K sums (this plan splits K) are
-    back to zero after each call."""
+    """out accumulates across calls; the BF16 route contributions at the start
+    of the workspace are scratch written before they are read (here they hold
+    garbage before the second call), and the split-K sums (this plan splits
+    K) are back to zero after each call."""
     cfg = SMALL["ragged_bm64"]
     prob = DeviceProblem(cfg)
     _run(prob, debug=False)
     once = prob.out.float().clone()
-    acc_bytes = cfg.M * cfg.H * 4
-    prob.workspace[:acc_bytes].fill_(0x7F)
+    y_bytes = cfg.R * cfg.H * 2
+    prob.workspace[:y_bytes].fill_(0x7F)
     prob.run_forward()
     torch.cuda.synchronize()
     twice = prob.out.float()
@@ -212,6 +212,69 @@ def test_plan_and_forward_replay_from_a_cuda_graph(name):
     assert int(prob.status.item()) == 0
 
 
+def _masked_reference(prob, kept):
+    """Oracle output from out_prior when only the routes in `kept` count."""
+    cfg = prob.cfg
+    ids = prob.routing.topk_ids.to(torch.int64).numpy().copy()
+    flat = ids.reshape(-1)
+    for r in range(flat.size):
+        if r not in kept:
+            flat[r] = -1
+    routing = W.Routing(torch.from_numpy(ids), prob.routing.topk_weights, prob.routing.zero_scale_experts)
+    inp, _ = oracle_inputs(cfg, routing, np.arange(cfg.M))
+    return O.moe_forward(**inp, routed_scale=cfg.routed_scale)
+
+
+def test_forward_ignores_routes_an_earlier_plan_held():
+    """A forward counts only the routes its own plan holds: routes that the
+    previous forward on this workspace held, and this plan drops (its extent
+    cut to the first block), contribute nothing."""
+    cfg = SMALL["ragged_bm64"]
+    prob = DeviceProblem(cfg)
+    _run(prob, debug=False)                      # every route held once
+    prob.out.copy_(prob.out_prior)
+    bm = cfg.block_m
+    kept = set(int(r) for r in prob.sorted_ids.cpu().numpy()[:bm] if r < cfg.R)
+    assert 0 < len(kept) < cfg.R
+    prob.ntpp.fill_(bm)
+    prob.run_forward()
+    torch.cuda.synchronize()
+    m = out_metrics(prob.out.float().cpu().numpy(), _masked_reference(prob, kept))
+    assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, m
+
+
+def test_graph_replays_follow_a_changing_plan():
+    """One captured plan + forward replayed with new expert ids each time:
+    every replay counts exactly the routes its own plan holds, including
+    after a replay that held more."""
+    cfg = SMALL["ragged_bm8"]
+    prob = DeviceProblem(cfg)
+    _run(prob, debug=False)
+    torch.cuda.synchronize()
+    args = prob.fwd_args()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            prob.run_plan()
+            prob.run_forward(args)
+    torch.cuda.current_stream().wait_stream(side)
+    full_ids = prob.topk_ids.clone()
+    R = cfg.R
+    for masked in ([], list(range(0, R, 2)), [], list(range(1, R, 3))):
+        ids = full_ids.clone()
+        ids.view(-1)[torch.as_tensor(masked, dtype=torch.long, device=ids.device)] = -1
+        prob.topk_ids.copy_(ids)
+        prob.out.copy_(prob.out_prior)
+        g.replay()
+        torch.cuda.synchronize()
+        kept = set(range(R)) - set(masked)
+        m = out_metrics(prob.out.float().cpu().numpy(), _masked_reference(prob, kept))
+        assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, (len(masked), m)
+    assert int(prob.status.item()) == 0
+
+
 def test_forward_all_masked_leaves_out_unchanged():
     cfg = SMALL["tiny"].with_(name="all_masked", masked_frac=1.0)
     prob = DeviceProblem(cfg)
@@ -233,16 +296,7 @@ def test_forward_truncated_extent_only_counts_leading_blocks():
     prob.ntpp.fill_(bm)
     prob.run_forward()
     torch.cuda.synchronize()
-    ids = prob.routing.topk_ids.to(torch.int64).numpy().copy()
-    flat = ids.reshape(-1)
-    for r in range(flat.size):
-        if r not in kept:
-            flat[r] = -1
-    routing = W.Routing(torch.from_numpy(ids), prob.routing.topk_weights, prob.routing.zero_scale_experts)
-    tokens = np.arange(cfg.M)
-    inp, _ = oracle_inputs(cfg, routing, tokens)
-    ref = O.moe_forward(**inp, routed_scale=cfg.routed_scale)
-    m = out_metrics(prob.out.float().cpu().numpy(), ref)
+    m = out_metrics(prob.out.float().cpu().numpy(), _masked_reference(prob, kept))
     assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, m
 
 
