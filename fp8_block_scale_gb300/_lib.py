@@ -62,7 +62,7 @@ class MoeFwdArgs(ctypes.Structure):
     ]
 
 
-TILE_AUTO, TILE_SINGLE, TILE_PAIR = 0, 1, 2
+TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_VECTOR = 0, 1, 2, 3
 
 
 _lib = None

@@ -279,6 +279,16 @@ __device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t v) {
   return __half22float2(h);
 }
 
+// Start moving `bytes` (a multiple of 16, 16-byte aligned) from global
+// memory into L2 without waiting for them.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// silu(g) = g / (1 + exp(-g)) with the hardware exp2 and divide
+// approximations (a few ulp; for g below about -88 the quotient is 0).
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }

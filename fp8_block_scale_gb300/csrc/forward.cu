@@ -18,8 +18,10 @@
 //      workspace.
 //   2. down (gemm kernel, kUp = false): intermediate rows x W2 tile, promoted
 //      with the intermediate and W2 block scales, times the route weight and
-//      routed scale, reduced into an FP32 [M, H] accumulator.
+//      routed scale, rounded to BF16 and stored as the route's row of the
+//      workspace (row index = route id).
 //   3. combine: out = bf16_rn(f32(out) + sum of the token's route rows).
+// Sparse plans (decode) take the vector path instead (vector.cu).
 //
 // The GEMM kernel is persistent and warp specialised (320 threads):
 //   warp 0      TMA producer: activation (or intermediate) rows, the 256-row
@@ -39,6 +41,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "vector.cuh"
 
 namespace moe {
 namespace {
@@ -181,10 +184,6 @@ __device__ __forceinline__ bool tile_coords(const GemmParams& p, const SmemCtl* 
   e = block_expert(p, ctl, b);
   return e >= 0 && e < p.E;
 }
-
-// silu(g) = g / (1 + exp(-g)) with the hardware exp2 and divide
-// approximations (a few ulp; for g below about -88 the quotient is 0).
-__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Plan entries of the four rows 4*lane .. 4*lane+3 of plan block b (gather4 path).
 __device__ __forceinline__ void load_ids(const GemmParams& p, int b, int lane, int (&id)[4]) {
@@ -937,8 +936,12 @@ int64_t block_bound(int64_t R, int E, int block_m) {
 // has SMs (decode-sized plans); the workspace then holds the partial sums.
 constexpr int64_t kSplitTileLimit = 256;
 
+// The automatic choice takes the vector path up to this many routes (at
+// 72 routes the tensor-core tiles are still faster).
+constexpr int64_t kVecAutoRoutes = 32;
+
 struct WsLayout {
-  size_t y_off, rv_off, gen_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, usum_off, ucnt_off, total;
+  size_t y_off, rv_off, gen_off, h_off, q_off, st_off, ast_off, tok_off, w_off, wsu_off, wsd_off, a_off, usum_off, ucnt_off, total;
   int64_t cap_pad, nblocks;
   bool pregather, splitk;
 };
@@ -960,6 +963,8 @@ WsLayout ws_layout(int64_t M, int H, int I, int E, int top_k, int block_m, int64
   l.y_off = take(R * H * 2);  // BF16 route contributions, by route id
   l.rv_off = take(R * 4);     // route flags: the stamp of the last forward whose plan held the route
   l.gen_off = take(4);        // the last forward's stamp
+  // vector path: silu(gate) * up in FP32 by route id
+  l.h_off = take(vector_path_supported(M, R, H, I) ? R * I * 4 : 0);
   l.q_off = take(sorted_cap * I);
   l.st_off = take(static_cast<int64_t>(nib) * l.cap_pad * 4);
   l.ast_off = take(static_cast<int64_t>(nkb) * l.cap_pad * 4);
@@ -1046,13 +1051,16 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       a->top_k > 64)
     return MOE_ERR_SHAPE;
   if (a->block_m < 8 || a->block_m > 128 || a->block_m % 8) return MOE_ERR_SHAPE;
-  if (a->tile_mode != MOE_TILE_AUTO && a->tile_mode != MOE_TILE_SINGLE && a->tile_mode != MOE_TILE_PAIR)
+  if (a->tile_mode != MOE_TILE_AUTO && a->tile_mode != MOE_TILE_SINGLE && a->tile_mode != MOE_TILE_PAIR &&
+      a->tile_mode != MOE_TILE_VECTOR)
     return MOE_ERR_SHAPE;
   if (a->blocks_cap < 1 || a->sorted_cap < a->blocks_cap * a->block_m) return MOE_ERR_CAPACITY;
   const int64_t R = a->M * a->top_k;
   if (R >= (int64_t(1) << 31) - 1 || static_cast<int64_t>(a->E) * 2 * a->I >= (int64_t(1) << 31) ||
       static_cast<int64_t>(a->E) * a->H >= (int64_t(1) << 31) || a->sorted_cap >= (int64_t(1) << 30))
     return MOE_ERR_SHAPE;
+  const bool vec_ok = vector_path_supported(a->M, R, a->H, a->I);
+  if (a->tile_mode == MOE_TILE_VECTOR && !vec_ok) return MOE_ERR_SHAPE;
   if (a->M == 0) return MOE_OK;
   if (!a->a || !a->a_scale || !a->w13 || !a->w13_scale || !a->w2 || !a->w2_scale || !a->topk_weights ||
       !a->sorted_token_ids || !a->expert_ids || !a->num_tokens_post_padded || !a->out || !a->workspace)
@@ -1092,6 +1100,55 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   const int N = 2 * a->I;
   int64_t nblocks = wl.nblocks;
   if (nblocks > a->blocks_cap) nblocks = a->blocks_cap;
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
+
+  // Sparse plans (a few routes per touched expert) take the vector path.
+  const bool use_vec = vec_ok && (a->tile_mode == MOE_TILE_VECTOR ||
+                                  (a->tile_mode == MOE_TILE_AUTO && R <= kVecAutoRoutes));
+  if (use_vec) {
+    float* hbuf = reinterpret_cast<float*>(ws + wl.h_off);
+    VecUpParams vu{};
+    vu.a = a->a;
+    vu.a_scale = a->a_scale;
+    vu.w13 = a->w13;
+    vu.w13_scale = a->w13_scale;
+    vu.sorted_ids = a->sorted_token_ids;
+    vu.expert_ids = a->expert_ids;
+    vu.num_post_padded = a->num_tokens_post_padded;
+    vu.h = hbuf;
+    vu.status = a->device_status;
+    vu.nblocks = nblocks;
+    vu.R = static_cast<int>(R);
+    vu.top_k = a->top_k;
+    vu.block_m = a->block_m;
+    vu.E = a->E;
+    vu.H = a->H;
+    vu.I = a->I;
+    VecDownParams vd{};
+    vd.h = hbuf;
+    vd.w2 = a->w2;
+    vd.w2_scale = a->w2_scale;
+    vd.topk_w = a->topk_weights;
+    vd.sorted_ids = a->sorted_token_ids;
+    vd.expert_ids = a->expert_ids;
+    vd.num_post_padded = a->num_tokens_post_padded;
+    vd.out = a->out;
+    vd.dbg_q = a->debug_q_inter;
+    vd.dbg_s = a->debug_s_inter;
+    vd.nblocks = nblocks;
+    vd.R = static_cast<int>(R);
+    vd.top_k = a->top_k;
+    vd.block_m = a->block_m;
+    vd.E = a->E;
+    vd.H = a->H;
+    vd.I = a->I;
+    vd.routed_scale = a->routed_scale;
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
+    const moe_status st = launch_vector_path(vu, vd, stream, ev);
+    if (st != MOE_OK) return st;
+    if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[4], stream));
+    return MOE_OK;
+  }
   // CTA pairs (cta_group::2) need the activation rows in plan order and the
   // expert and pair tables in shared memory.  Each SM then streams half of
   // every weight tile, but per K slice the pair runs no faster than a single
@@ -1116,7 +1173,6 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
 
-  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->profile_events);
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
   if (nblocks > 0) {
     StageParams sp{};

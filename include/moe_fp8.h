@@ -217,21 +217,35 @@ typedef struct moe_fwd_args {
   int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
 } moe_fwd_args;
 
-/* tile_mode values.  Every mode computes the same result.
- *   MOE_TILE_AUTO   the library chooses (currently always one CTA per tile).
+/* tile_mode values.  Every mode computes the same result (up to FP32
+ * summation order).
+ *   MOE_TILE_AUTO   the library chooses: the vector path for sparse plans
+ *                   (M * top_k <= 32 routes, where it is supported), else
+ *                   one CTA per tile.
  *   MOE_TILE_SINGLE one CTA per 128-row tile (cta_group::1 MMAs).
  *   MOE_TILE_PAIR   two CTAs of a cluster per pair of plan blocks of one
  *                   expert (cta_group::2, M = 256): each CTA streams half of
  *                   the weight tile.  Used where the plan qualifies (activation
  *                   rows copied into plan order and at most 1024 plan blocks),
  *                   otherwise the forward falls back to MOE_TILE_SINGLE.
+ *   MOE_TILE_VECTOR the vector path for decode-sized plans: the two
+ *                   projections as matrix-vector products on the CUDA cores
+ *                   (two launches, no staging or combine launch; each
+ *                   route's contributions are added to f32(out) in FP32
+ *                   without a BF16 rounding of their own).  Supported for
+ *                   M * top_k <= 1024, M <= 64 and I <= 1024; otherwise this
+ *                   mode returns MOE_ERR_SHAPE.  A plan that holds one route
+ *                   in two slots is malformed; this path counts the route at
+ *                   its first slot.
  * Any other value returns MOE_ERR_SHAPE. */
 #define MOE_TILE_AUTO 0
 #define MOE_TILE_SINGLE 1
 #define MOE_TILE_PAIR 2
+#define MOE_TILE_VECTOR 3
 
 /* Workspace bytes the forward needs (host-only; 0 for invalid sizes).  The
- * workspace holds the BF16 route contributions [M * top_k, H], the requantised
+ * workspace holds the BF16 route contributions [M * top_k, H], for problems
+ * the vector path supports its FP32 SwiGLU output [M * top_k, I], the requantised
  * intermediate (sorted_cap x I codes and sorted_cap x I/128 scales) and, for
  * well-filled plans (M * top_k >= 8 * min(E, M * top_k)), the activation rows
  * and scales copied into plan order (sorted_cap x H bytes and

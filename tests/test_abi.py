@@ -89,9 +89,15 @@ def test_forward_host_validation_without_gpu(lib):
     a.block_m = 256
     assert f(ctypes.byref(a), None) == 2                         # block_m > 128
     a.block_m = 64
-    for bad in (-1, 3):
+    for bad in (-1, 4):
         a.tile_mode = bad
         assert f(ctypes.byref(a), None) == 2                     # unknown tile mode
+    a.tile_mode = 3                                              # the vector path ...
+    a.M = 65
+    assert f(ctypes.byref(a), None) == 2                         # ... takes at most 64 tokens
+    a.M, a.I = 4, 1152
+    assert f(ctypes.byref(a), None) == 2                         # ... and I <= 1024
+    a.I = 256
     a.tile_mode = 2
     a.sorted_cap = 639
     assert f(ctypes.byref(a), None) == 4                         # capacity

@@ -96,6 +96,21 @@ def test_forward_small_all_tokens(name):
     assert int(prob.status.item()) == 0
 
 
+# the vector path takes at most 64 tokens
+VECTOR_SMALL = [n for n, c in SMALL.items() if c.M <= 64]
+
+
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+@pytest.mark.parametrize("name", VECTOR_SMALL)
+def test_forward_small_each_path(name, mode):
+    """Both the tensor-core tiles and the vector path on every small case the
+    vector path supports (the automatic choice takes one of them)."""
+    prob = DeviceProblem(SMALL[name])
+    dq, ds = _run(prob, tile_mode=mode)
+    _check(prob, np.arange(prob.cfg.M), dq, ds, f"mode{mode}")
+    assert int(prob.status.item()) == 0
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled tokens
 
 FULL = {
@@ -129,6 +144,14 @@ def test_forward_full_size_sampled(name):
     _full_size(name, L.TILE_AUTO)
 
 
+@pytest.mark.parametrize("name,mode", [("decode_m1", L.TILE_SINGLE), ("decode_m8", L.TILE_SINGLE),
+                                       ("decode_m64", L.TILE_VECTOR)], ids=["m1-single", "m8-single", "m64-vector"])
+def test_forward_decode_other_path(name, mode):
+    """The decode workloads through the path the automatic choice does not
+    take for them."""
+    _full_size(name, mode)
+
+
 # ------------------------------------------------------------------ CTA pairs (cta_group::2)
 
 # Plans with the activation rows in plan order qualify for CTA pairs: blocks
@@ -151,12 +174,14 @@ def test_forward_full_size_cta_pairs(name):
     _full_size(name, L.TILE_PAIR)
 
 
-def test_forward_modes_agree():
-    """Single CTAs and CTA pairs give the same intermediate codes and outputs
-    up to FP32 summation order."""
-    cfg = SMALL["hot_many_blocks"]
+@pytest.mark.parametrize("name,modes", [("hot_many_blocks", (L.TILE_SINGLE, L.TILE_PAIR)),
+                                        ("masked_zero", (L.TILE_SINGLE, L.TILE_VECTOR))], ids=["pair", "vector"])
+def test_forward_modes_agree(name, modes):
+    """Single CTAs, CTA pairs and the vector path give the same intermediate
+    codes and outputs up to FP32 summation order."""
+    cfg = SMALL[name]
     outs = []
-    for mode in (L.TILE_SINGLE, L.TILE_PAIR):
+    for mode in modes:
         prob = DeviceProblem(cfg)
         dq, _ = _run(prob, tile_mode=mode)
         outs.append((prob.out.float().cpu(), dq.cpu().numpy()))
@@ -168,18 +193,19 @@ def test_forward_modes_agree():
 
 # ------------------------------------------------------------------ semantics
 
-def test_forward_accumulates_and_reuses_its_workspace():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_forward_accumulates_and_reuses_its_workspace(mode):
     """out accumulates across calls; the BF16 route contributions at the start
     of the workspace are scratch written before they are read (here they hold
     garbage before the second call), and the split-K sums (this plan splits
     K) are back to zero after each call."""
     cfg = SMALL["ragged_bm64"]
     prob = DeviceProblem(cfg)
-    _run(prob, debug=False)
+    _run(prob, debug=False, tile_mode=mode)
     once = prob.out.float().clone()
     y_bytes = cfg.R * cfg.H * 2
     prob.workspace[:y_bytes].fill_(0x7F)
-    prob.run_forward()
+    prob.run_forward(prob.fwd_args(tile_mode=mode))
     torch.cuda.synchronize()
     twice = prob.out.float()
     delta1 = once - prob.out_prior.float()
@@ -188,16 +214,17 @@ def test_forward_accumulates_and_reuses_its_workspace():
     assert rel < 2e-2, rel.item()
 
 
-@pytest.mark.parametrize("name", ["ragged_bm64", "ragged_bm128"])
-def test_plan_and_forward_replay_from_a_cuda_graph(name):
+@pytest.mark.parametrize("name,mode", [("ragged_bm64", L.TILE_SINGLE), ("ragged_bm128", L.TILE_AUTO),
+                                       ("ragged_bm64", L.TILE_VECTOR)], ids=["splitk", "pregather", "vector"])
+def test_plan_and_forward_replay_from_a_cuda_graph(name, mode):
     """Every call the library makes while launching is legal under stream
     capture: plan + forward captured once and replayed give the oracle's
     result (split K on the first case, plan-ordered rows on the second)."""
     prob = DeviceProblem(SMALL[name])
-    _run(prob, debug=False)                      # first calls set the kernels' attributes
+    _run(prob, debug=False, tile_mode=mode)      # first calls set the kernels' attributes
     torch.cuda.synchronize()
     prob.out.copy_(prob.out_prior)
-    args = prob.fwd_args()
+    args = prob.fwd_args(tile_mode=mode)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -225,33 +252,35 @@ def _masked_reference(prob, kept):
     return O.moe_forward(**inp, routed_scale=cfg.routed_scale)
 
 
-def test_forward_ignores_routes_an_earlier_plan_held():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_forward_ignores_routes_an_earlier_plan_held(mode):
     """A forward counts only the routes its own plan holds: routes that the
     previous forward on this workspace held, and this plan drops (its extent
     cut to the first block), contribute nothing."""
     cfg = SMALL["ragged_bm64"]
     prob = DeviceProblem(cfg)
-    _run(prob, debug=False)                      # every route held once
+    _run(prob, debug=False, tile_mode=mode)      # every route held once
     prob.out.copy_(prob.out_prior)
     bm = cfg.block_m
     kept = set(int(r) for r in prob.sorted_ids.cpu().numpy()[:bm] if r < cfg.R)
     assert 0 < len(kept) < cfg.R
     prob.ntpp.fill_(bm)
-    prob.run_forward()
+    prob.run_forward(prob.fwd_args(tile_mode=mode))
     torch.cuda.synchronize()
     m = out_metrics(prob.out.float().cpu().numpy(), _masked_reference(prob, kept))
     assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, m
 
 
-def test_graph_replays_follow_a_changing_plan():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_graph_replays_follow_a_changing_plan(mode):
     """One captured plan + forward replayed with new expert ids each time:
     every replay counts exactly the routes its own plan holds, including
     after a replay that held more."""
     cfg = SMALL["ragged_bm8"]
     prob = DeviceProblem(cfg)
-    _run(prob, debug=False)
+    _run(prob, debug=False, tile_mode=mode)
     torch.cuda.synchronize()
-    args = prob.fwd_args()
+    args = prob.fwd_args(tile_mode=mode)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -275,16 +304,18 @@ def test_graph_replays_follow_a_changing_plan():
     assert int(prob.status.item()) == 0
 
 
-def test_forward_all_masked_leaves_out_unchanged():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_forward_all_masked_leaves_out_unchanged(mode):
     cfg = SMALL["tiny"].with_(name="all_masked", masked_frac=1.0)
     prob = DeviceProblem(cfg)
     assert (prob.routing.topk_ids == -1).all()
-    _run(prob, debug=False)
+    _run(prob, debug=False, tile_mode=mode)
     assert torch.equal(prob.out.view(torch.int16), prob.out_prior.view(torch.int16))
     assert int(prob.ntpp.item()) == 0
 
 
-def test_forward_truncated_extent_only_counts_leading_blocks():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_forward_truncated_extent_only_counts_leading_blocks(mode):
     """Blocks at and past num_tokens_post_padded exit untouched."""
     cfg = SMALL["ragged_bm64"]
     prob = DeviceProblem(cfg)
@@ -294,19 +325,20 @@ def test_forward_truncated_extent_only_counts_leading_blocks():
     sorted_ids = prob.sorted_ids.cpu().numpy()
     kept = set(int(r) for r in sorted_ids[:bm] if r < cfg.R)
     prob.ntpp.fill_(bm)
-    prob.run_forward()
+    prob.run_forward(prob.fwd_args(tile_mode=mode))
     torch.cuda.synchronize()
     m = out_metrics(prob.out.float().cpu().numpy(), _masked_reference(prob, kept))
     assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, m
 
 
-def test_forward_reports_bad_expert_in_plan():
+@pytest.mark.parametrize("mode", [L.TILE_SINGLE, L.TILE_VECTOR], ids=["single", "vector"])
+def test_forward_reports_bad_expert_in_plan(mode):
     cfg = SMALL["tiny"]
     prob = DeviceProblem(cfg)
     prob.run_plan()
     torch.cuda.synchronize()
     prob.expert_ids[0] = cfg.E + 3                         # corrupt one block of the plan
-    prob.run_forward()
+    prob.run_forward(prob.fwd_args(tile_mode=mode))
     torch.cuda.synchronize()
     assert int(prob.status.item()) & L.MOE_DEV_BAD_EXPERT
     assert torch.isfinite(prob.out.float()).all()
