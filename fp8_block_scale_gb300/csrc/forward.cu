@@ -1112,6 +1112,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     vu.a_scale = a->a_scale;
     vu.w13 = a->w13;
     vu.w13_scale = a->w13_scale;
+    vu.w2 = a->w2;
     vu.sorted_ids = a->sorted_token_ids;
     vu.expert_ids = a->expert_ids;
     vu.num_post_padded = a->num_tokens_post_padded;

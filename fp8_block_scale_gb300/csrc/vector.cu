@@ -95,8 +95,18 @@ __global__ void __launch_bounds__(32 * kUpWarps, 4) vec_up_kernel(const VecUpPar
   pdl_wait();
   // the down kernel reads the plan before its own wait: release it only now
   pdl_launch_dependents();
-  if (b >= valid_blocks(p.num_post_padded, p.block_m, p.nblocks)) return;
+  // extent, expert and the block's route ids in one round trip (slots of
+  // blocks inside the plan capacity are always readable)
+  int ids[4];
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int sl = 32 * i + lane;
+      ids[i] = sl < p.block_m ? __ldcg(p.sorted_ids + b * p.block_m + sl) : -1;
+    }
+  }
   const int e = __ldcg(p.expert_ids + b);
+  if (b >= valid_blocks(p.num_post_padded, p.block_m, p.nblocks)) return;
   if (e < 0 || e >= p.E) {
     if (e != -1 && c0 == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, MOE_DEV_BAD_EXPERT);
     return;
@@ -108,15 +118,21 @@ __global__ void __launch_bounds__(32 * kUpWarps, 4) vec_up_kernel(const VecUpPar
     // into L2 now, ahead of the warps' own loads
     prefetch_l2_bulk(wg, 4u * p.H);
     prefetch_l2_bulk(wg + 8 * static_cast<int64_t>(p.H), 4u * p.H);
+  } else if (threadIdx.x == 64) {
+    // and this CTA's share of the expert's W2 rows, which the down kernel
+    // reads next (the block's quads split the expert's H x I bytes)
+    const int64_t w2b = static_cast<int64_t>(p.H) * p.I;
+    const int64_t share = (w2b / quads + 15) / 16 * 16;
+    const int64_t off = (blockIdx.x % quads) * share;
+    if (off < w2b) prefetch_l2_bulk(p.w2 + e * w2b + off, static_cast<uint32_t>(off + share <= w2b ? share : w2b - off));
   }
   if (warp == 0) {
     int n = 0;
-    for (int i0 = 0; i0 < p.block_m; i0 += 32) {
-      const int i = i0 + lane;
-      const int id = i < p.block_m ? __ldcg(p.sorted_ids + b * p.block_m + i) : -1;
-      const bool route = id >= 0 && id < p.R;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool route = ids[i] >= 0 && ids[i] < p.R;
       const unsigned m = __ballot_sync(0xffffffffu, route);
-      if (route) s_route[n + __popc(m & ((1u << lane) - 1u))] = id;
+      if (route) s_route[n + __popc(m & ((1u << lane) - 1u))] = ids[i];
       n += __popc(m);
     }
     if (lane == 0) s_nr = n;
@@ -218,6 +234,7 @@ struct DownSmem {
     } b;
   } u;
   HeldRoute held[kVecMaxRoutes];
+  float weight[kVecMaxRoutes];        // topk_weights * routed_scale of every route
   float acc[kVecMaxTokens][kDnRows];  // f32(out) plus the contributions so far
   int nheld;
   int wcount[4];
@@ -237,15 +254,35 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
 
   // 1. Routes the plan holds (read before the wait: the plan is an input,
   //    complete before the gate/up kernel released this grid).
-  for (int r = threadIdx.x; r < p.R; r += nthreads) sm.u.map[r] = ~0ull;
+  for (int r = threadIdx.x; r < p.R; r += nthreads) {
+    sm.u.map[r] = ~0ull;
+    sm.weight[r] = __fmul_rn(__ldcg(p.topk_w + r), p.routed_scale);
+  }
   if (threadIdx.x == 0) sm.nheld = 0;
   __syncthreads();
-  const int64_t nslots = valid_blocks(p.num_post_padded, p.block_m, p.nblocks) * p.block_m;
-  for (int64_t s = threadIdx.x; s < nslots; s += nthreads) {
-    const int id = __ldcg(p.sorted_ids + s);
-    const int e = __ldcg(p.expert_ids + s / p.block_m);
-    if (id >= 0 && id < p.R && e >= 0 && e < p.E)
-      atomicMin(&sm.u.map[id], (static_cast<unsigned long long>(s) << 32) | static_cast<uint32_t>(e));
+  // every slot of the plan's capacity is read, eight per thread at a time,
+  // with the extent loaded alongside and checked afterwards
+  {
+    constexpr int kScan = 8;
+    const int64_t P = __ldcg(p.num_post_padded);
+    const int64_t cap_slots = p.nblocks * p.block_m;
+    for (int64_t s0 = threadIdx.x; s0 < cap_slots; s0 += kScan * nthreads) {
+      int id[kScan], ex[kScan];
+#pragma unroll
+      for (int k = 0; k < kScan; ++k) {
+        const int64_t sl = s0 + k * nthreads;
+        id[k] = sl < cap_slots ? __ldcg(p.sorted_ids + sl) : -1;
+        ex[k] = sl < cap_slots ? __ldcg(p.expert_ids + sl / p.block_m) : -1;
+      }
+      int64_t nvalid = (P < 0 ? 0 : P) / p.block_m;
+      if (nvalid > p.nblocks) nvalid = p.nblocks;
+#pragma unroll
+      for (int k = 0; k < kScan; ++k) {
+        const int64_t sl = s0 + k * nthreads;
+        if (sl < nvalid * p.block_m && id[k] >= 0 && id[k] < p.R && ex[k] >= 0 && ex[k] < p.E)
+          atomicMin(&sm.u.map[id[k]], (static_cast<unsigned long long>(sl) << 32) | static_cast<uint32_t>(ex[k]));
+      }
+    }
   }
   __syncthreads();
   // compact in route order (token-major), 128 routes per round
@@ -263,7 +300,7 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
       h.route = r;
       h.slot = static_cast<int>(v >> 32);
       h.expert = static_cast<int>(v & 0xFFFFFFFFu);
-      h.weight = __fmul_rn(__ldcg(p.topk_w + r), p.routed_scale);
+      h.weight = sm.weight[r];
       sm.held[off + __popc(m & ((1u << lane) - 1u))] = h;
     }
     __syncthreads();
@@ -304,20 +341,16 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
   pdl_wait();
   pdl_launch_dependents();
 
-  // 3. f32(out) of every token of the list, for this CTA's rows
   const int64_t tok_lo = nh > 0 ? sm.held[0].route / p.top_k : 0;
   const int ntok = nh > 0 ? static_cast<int>(sm.held[nh - 1].route / p.top_k - tok_lo) + 1 : 0;
-  for (int i = threadIdx.x; i < ntok * kDnRows; i += nthreads) {
-    const int tt = i / kDnRows, rr = i % kDnRows;
-    const int orow = row0 + rr;
-    sm.acc[tt][rr] = orow < p.H ? __bfloat162float(__ushort_as_bfloat16(p.out[(tok_lo + tt) * p.H + orow])) : 0.f;
-  }
 
   for (int j0 = 0; j0 < nh; j0 += kJB) {
-    if (j0 > 0) load_batch(j0);
-    __syncthreads();  // acc initialised; the previous batch's q no longer read
-    // 4. requantise the batch's intermediate rows (a warp per route), every
-    //    row's loads issued before any is used
+    if (j0 > 0) {
+      load_batch(j0);
+      __syncthreads();  // the previous batch's q is no longer read
+    }
+    // 3. the batch's intermediate rows (a warp per route), every row's loads
+    //    issued before any is used
     const int nb = nh - j0 < kJB ? nh - j0 : kJB;
     float4 hv[kRq][kU];
 #pragma unroll
@@ -329,6 +362,18 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
         hv[i][g] = jj < nb ? __ldcg(reinterpret_cast<const float4*>(hrow + 128 * g) + lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (j0 == 0) {
+      // f32(out) of every token of the list, for this CTA's rows (these
+      // loads overlap the ones above; the barrier after the requant
+      // publishes them)
+      for (int i = threadIdx.x; i < ntok * kDnRows; i += nthreads) {
+        const int tt = i / kDnRows, rr = i % kDnRows;
+        const int orow = row0 + rr;
+        sm.acc[tt][rr] =
+            orow < p.H ? __bfloat162float(__ushort_as_bfloat16(p.out[(tok_lo + tt) * p.H + orow])) : 0.f;
+      }
+    }
+    // 4. requantise
 #pragma unroll
     for (int i = 0; i < kRq; ++i) {
       const int jj = warp + 4 * i;

@@ -15,6 +15,7 @@ struct VecUpParams {
   const float* a_scale;             // [M, H/128]
   const uint8_t* w13;               // [E, 2I, H] interleaved E4M3
   const float* w13_scale;           // [E, 2I/128, H/128] logical row blocks
+  const uint8_t* w2;                // [E, H, I]: the expert's rows are prefetched into L2
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* num_post_padded;
