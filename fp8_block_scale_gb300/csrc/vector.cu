@@ -1,19 +1,22 @@
 // The vector path of moe_fp8_block_scale_forward, for sparse plans (decode:
 // one or two routes per touched expert).  With so few activation rows per
-// expert both projections are matrix-vector products whose cost is the
-// weight stream itself (FlashInfer PR #4287 perf notes: decode-size calls are
-// bound by weight bytes), so they run on the CUDA cores as plain 16-byte
-// loads with FP32 FMAs instead of 128-row tensor-core tiles: no staging
-// launch, no TMA ring to fill per tile, and the down projection loads its
-// weights before it waits for the gate/up kernel.
+// expert both projections are matrix-vector products: two FLOP per weight
+// byte and route, so their cost is the weight stream itself.  They run on
+// the CUDA cores as plain 16-byte loads with FP32 FMAs instead of 128-row
+// tensor-core tiles: no staging launch, no TMA ring to fill per tile, and the
+// down projection lists its routes and loads its weights before it waits for
+// the gate/up kernel.
 //
 // Launches (programmatic dependent launch between them):
 //   1. vec_up_kernel: a CTA per (plan block, 4 intermediate columns).  Its
-//      four warps stream the 8 interleaved W13 rows of those columns (4 gate,
-//      4 up; 2 rows per warp) over the whole of K, multiply each 16-code
-//      partial by the activation and weight block scales of its 128-wide K
-//      slice, and write silu(gate) * up in FP32 for every route of the block
-//      to h[route, I].
+//      eight warps (4 row pairs x 2 halves of K) stream the 8 interleaved
+//      W13 rows of those columns (4 gate, 4 up; a bulk L2 prefetch starts
+//      them at once) against the route's activation row, converted once to
+//      FP32 in shared memory; each 16-code partial is multiplied by the
+//      activation and weight block scales of its 128-wide K slice, and
+//      silu(gate) * up is written in FP32 for every route of the block to
+//      h[route, I].  The CTA also prefetches its share of the expert's W2
+//      rows into L2 for the down kernel.
 //   2. vec_down_kernel: a CTA per 16 output columns, for all tokens.  It
 //      reads the plan to list the held routes in route order (the plan is
 //      complete before the forward starts) and loads the first routes' W2

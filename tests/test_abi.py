@@ -97,7 +97,11 @@ def test_forward_host_validation_without_gpu(lib):
     assert f(ctypes.byref(a), None) == 2                         # ... takes at most 64 tokens
     a.M, a.I = 4, 1152
     assert f(ctypes.byref(a), None) == 2                         # ... and I <= 1024
-    a.I = 256
+    a.M, a.I, a.top_k = 64, 256, 17
+    assert f(ctypes.byref(a), None) == 2                         # ... and M * top_k <= 1024 routes
+    a.M, a.top_k, a.H = 4, 2, 8320
+    assert f(ctypes.byref(a), None) == 2                         # ... and H <= 8192
+    a.H = 256
     a.tile_mode = 2
     a.sorted_cap = 639
     assert f(ctypes.byref(a), None) == 4                         # capacity
