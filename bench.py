@@ -617,6 +617,22 @@ def extra_sweep(cfg, prob, flush, peaks):
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
                                     "combine": r["combine_ms"]}}
         del p
+    # the other two workloads at their own sizes and weights
+    for name in ("skewed", "large"):
+        c = W.CONFIGS[name]
+        p = DeviceProblem(c)
+        r = measure(p, 10, 3, flush)
+        w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
+        t_flop = w["total"]["flop"] / (fp8_peak * 1e12)
+        t_bytes = w["total"]["bytes"] / (hbm * 1e9)
+        out[name] = {"ms_step": r["step_ms"], "ms_forward": r["forward_ms"], "ms_plan": r["plan_ms"],
+                     "tflops_forward": w["total"]["flop"] / (r["forward_ms"] * 1e-3) / 1e12,
+                     "t_flop_us": t_flop * 1e6, "t_bytes_us": t_bytes * 1e6,
+                     "frac_roofline_forward": max(t_flop, t_bytes) / (r["forward_ms"] * 1e-3),
+                     "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
+                                    "combine": r["combine_ms"]}}
+        del p
+        torch.cuda.empty_cache()
     base = None
     for name in ("decode_m1", "decode_m8", "decode_m64"):
         c = W.CONFIGS[name]
