@@ -84,6 +84,8 @@ _SIGS = {
                                       ctypes.c_void_p]),
     "moe_quantize_act_1x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_quantize_act_1x128_ue8m0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                                    ctypes.c_void_p, ctypes.c_void_p]),
     "moe_quantize_weight_128x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_forward_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -176,6 +178,12 @@ def moe_route_topk(logits, top_k, topk_ids, topk_weights, routed_scale=1.0, reno
 def moe_quantize_act_1x128(x_bf16, q, scale, stream=None):
     M, H = x_bf16.shape
     _check("moe_quantize_act_1x128", load().moe_quantize_act_1x128(
+        _ptr(x_bf16), M, H, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_act_1x128_ue8m0(x_bf16, q, scale, stream=None):
+    M, H = x_bf16.shape
+    _check("moe_quantize_act_1x128_ue8m0", load().moe_quantize_act_1x128_ue8m0(
         _ptr(x_bf16), M, H, _ptr(q), _ptr(scale), _stream(stream)))
 
 

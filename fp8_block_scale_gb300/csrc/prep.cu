@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(256) requant_ue8m0_kernel(uint8_t* __restrict_
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
 // One warp per (row, 128-column group): lane l holds columns 4l..4l+3.
+// kPow2: the group's scale amax/448 is rounded up to a power of two (UE8M0),
+// as the weight requant rounds block scales.
+template <bool kPow2>
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int H,
                                                         uint8_t* __restrict__ q, float* __restrict__ scale) {
   const int groups = H / 128;
@@ -123,7 +126,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
   float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 448.0f);
+  float s = __fdiv_rn(amax, 448.0f);
+  if (kPow2 && s > 0.f) s = pow2_round_up(s);
   uint32_t packed = 0;
   if (s > 0.f) {
     const uint16_t lo = cvt_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s));
@@ -200,6 +204,27 @@ int grid_for(int64_t work, int threads, int sms) {
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+template <bool kPow2>
+moe_status quantize_act(const uint16_t* x, int64_t M, int H, uint8_t* q, float* scale, cudaStream_t stream) {
+  if (M == 0) return MOE_OK;
+  if (!x || !q || !scale) return MOE_ERR_NULL;
+  if (M < 0 || H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q)) return MOE_ERR_ALIGN;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if (!on_device(x, dev.device) || !on_device(q, dev.device) || !on_device(scale, dev.device)) return MOE_ERR_DEVICE;
+  const int64_t warps = M * (H / 128);
+  const int64_t blocks = ceil_div(warps * 32, 256);
+  if (blocks > 0x7FFFFFFF) return MOE_ERR_SHAPE;
+  quant_act_kernel<kPow2><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, M, H, q, scale);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_prep_weights(const uint8_t* w13, uint8_t* w13_interleaved, int E, int N, int H, moe_stream_t stream) {
@@ -238,21 +263,14 @@ moe_status moe_requant_scales_ue8m0(uint8_t* w, float* scale, uint8_t* ue8m0_exp
   return MOE_OK;
 }
 
+
 moe_status moe_quantize_act_1x128(const uint16_t* x, int64_t M, int H, uint8_t* q, float* scale, moe_stream_t stream) {
-  using namespace moe;
-  if (M == 0) return MOE_OK;
-  if (!x || !q || !scale) return MOE_ERR_NULL;
-  if (M < 0 || H < 128 || H % 128 != 0) return MOE_ERR_SHAPE;
-  if (!aligned16(x) || !aligned16(q)) return MOE_ERR_ALIGN;
-  DeviceInfo dev;
-  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
-  if (!on_device(x, dev.device) || !on_device(q, dev.device) || !on_device(scale, dev.device)) return MOE_ERR_DEVICE;
-  const int64_t warps = M * (H / 128);
-  const int64_t blocks = ceil_div(warps * 32, 256);
-  if (blocks > 0x7FFFFFFF) return MOE_ERR_SHAPE;
-  quant_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, M, H, q, scale);
-  MOE_CUDA_TRY(cudaGetLastError());
-  return MOE_OK;
+  return moe::quantize_act<false>(x, M, H, q, scale, stream);
+}
+
+moe_status moe_quantize_act_1x128_ue8m0(const uint16_t* x, int64_t M, int H, uint8_t* q, float* scale,
+                                        moe_stream_t stream) {
+  return moe::quantize_act<true>(x, M, H, q, scale, stream);
 }
 
 moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, int cols, uint8_t* q, float* scale,

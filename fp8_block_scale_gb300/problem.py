@@ -32,7 +32,10 @@ class DeviceProblem:
         x = W.make_activations(cfg, device=dev)
         self.a = torch.empty(M, H, dtype=torch.uint8, device=dev)
         self.a_scale = torch.empty(M, H // 128, dtype=torch.float32, device=dev)
-        L.moe_quantize_act_1x128(x, self.a, self.a_scale)
+        if cfg.act_ue8m0:
+            L.moe_quantize_act_1x128_ue8m0(x, self.a, self.a_scale)
+        else:
+            L.moe_quantize_act_1x128(x, self.a, self.a_scale)
         del x
 
         if weights_from is not None:

@@ -46,7 +46,8 @@ class MoEConfig:
     routing: str = "uniform"          # "softmax_topk" | "uniform" | "skewed"
     out_init: str = "zero"            # "zero" | "normal0.1"
     id_dtype: torch.dtype = torch.int32
-    ue8m0: bool = False
+    ue8m0: bool = False               # weight block scales requantised to powers of two
+    act_ue8m0: bool = False           # activations quantised with power-of-two group scales
     routed_scale: float = 1.0
     garbage_plan: bool = False        # fill plan buffers with random bits first
     masked_frac: float = 0.0

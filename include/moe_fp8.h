@@ -132,6 +132,14 @@ moe_status moe_requant_scales_ue8m0(uint8_t* w, float* scale, uint8_t* ue8m0_exp
 moe_status moe_quantize_act_1x128(const uint16_t* x, int64_t M, int H,
                                   uint8_t* q, float* scale, moe_stream_t stream);
 
+/* The same with power-of-two (UE8M0) group scales, the form a hardware
+ * block-scaled MMA consumes: each group's scale amax/448 is rounded up to the
+ * smallest power of two not below it (as moe_requant_scales_ue8m0 rounds
+ * weight block scales; a scale above 2^127 is kept), so codes stay within
+ * +-448 and divide exactly.  Scales are still written as FP32. */
+moe_status moe_quantize_act_1x128_ue8m0(const uint16_t* x, int64_t M, int H,
+                                        uint8_t* q, float* scale, moe_stream_t stream);
+
 /* w [E, rows, cols] BF16 bits -> q [E, rows, cols] E4M3,
  * scale [E, rows/128, cols/128] FP32.  rows, cols % 128 == 0. */
 moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, int cols,

@@ -37,7 +37,7 @@ def oracle_inputs(cfg, routing, tokens, device=None):
     remap = {e: i for i, e in enumerate(experts)}
     ids_c = np.array([[remap.get(int(e), -1) for e in row] for row in ids], dtype=np.int64)
     x = W.make_activations(cfg, device=device)[torch.as_tensor(tokens, device=device)].float().cpu().numpy()
-    a_q, a_s = O.quantize_act_1x128(x)
+    a_q, a_s = O.quantize_act_1x128_ue8m0(x) if cfg.act_ue8m0 else O.quantize_act_1x128(x)
     w13_q, w13_s, w2_q, w2_s = [], [], [], []
     for e in experts:
         q, s = O.quantize_weight_128x128(W.make_expert_weights(cfg, e, "w13", device).float().cpu().numpy()[None])

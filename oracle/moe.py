@@ -96,6 +96,27 @@ def quantize_act_1x128(x):
     return codes.reshape(M, H), scale
 
 
+def quantize_act_1x128_ue8m0(x):
+    """Per-token 1x128 activation quantisation with power-of-two (UE8M0)
+    scales: each group's amax/448 rounded up to a power of two, the rounding
+    the UE8M0 requant applies to weight block scales ([SGL-43556]; "rounded
+    up", reading 15), so that both operands' scales are powers of two as a
+    hardware block-scaled MMA requires.  Codes are E4M3(f32(x / scale)).
+
+    x: float32 [M, H] (BF16 values) -> (codes uint8 [M, H], scale float32
+    [M, H/128]); an all-zero group gets scale 0 and zero codes.
+    """
+    x = f32(x)
+    M, H = x.shape
+    assert H % GROUP == 0
+    g = x.reshape(M, H // GROUP, GROUP)
+    scale = ue8m0_round_up(f32(np.max(np.abs(g), axis=-1) / np.float32(E4M3_MAX)))
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = e4m3_encode(f32(g / safe[..., None]))
+    codes = np.where((scale > 0)[..., None], codes, np.uint8(0)).astype(np.uint8)
+    return codes.reshape(M, H), scale
+
+
 def quantize_weight_128x128(w):
     """128x128 block weight quantisation ([FI-4287 contract]).
 

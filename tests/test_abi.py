@@ -131,6 +131,8 @@ def test_plan_and_prep_host_validation_without_gpu(lib):
     assert lib.moe_prep_weights(p, p, 2, 256, 128, None) == 2                             # overlap
     assert lib.moe_requant_scales_ue8m0(p, p, None, 1, 100, 128, None) == 2
     assert lib.moe_quantize_act_1x128(p, 4, 100, p, p, None) == 2
+    assert lib.moe_quantize_act_1x128_ue8m0(p, 4, 100, p, p, None) == 2
+    assert lib.moe_quantize_act_1x128_ue8m0(None, 4, 128, p, p, None) == 1
     assert lib.moe_quantize_weight_128x128(p, 1, 128, 64, p, p, None) == 2
 
 

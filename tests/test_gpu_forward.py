@@ -85,6 +85,9 @@ SMALL = {
     "ue8m0_small": W.MoEConfig("ue8m0_small", M=40, H=384, I=128, E=4, top_k=2, block_m=64, ue8m0=True,
                                out_init="normal0.1"),
     "h_odd_tiles": W.MoEConfig("h_odd_tiles", M=20, H=640, I=128, E=3, top_k=2, block_m=32),
+    # power-of-two scales on both operands (the form a hardware block-scaled MMA takes)
+    "ue8m0_both": W.MoEConfig("ue8m0_both", M=40, H=384, I=256, E=4, top_k=2, block_m=64, ue8m0=True,
+                              act_ue8m0=True, out_init="normal0.1"),
 }
 
 

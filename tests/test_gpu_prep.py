@@ -38,6 +38,23 @@ def test_quantize_act_bit_exact(M, H):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+@pytest.mark.parametrize("M,H", [(1, 128), (37, 384), (300, 7168)])
+def test_quantize_act_ue8m0_bit_exact(M, H):
+    rng = np.random.default_rng(M * 3 + H)
+    x = _bf16(rng, (M, H), 1.0)
+    x[M // 2, :128] = 0                                   # an all-zero group
+    x[0, 5] = 1e-30                                       # a value far below the group's scale
+    x[-1, :128] = torch.from_numpy(bf16_round(rng.uniform(-13, 13, 128).astype(np.float32))).to(torch.bfloat16)
+    x[-1, 3] = 14.0                                       # amax/448 = 2^-5: already a power of two
+    q = torch.empty(M, H, dtype=torch.uint8, device="cuda")
+    s = torch.empty(M, H // 128, dtype=torch.float32, device="cuda")
+    L.moe_quantize_act_1x128_ue8m0(x.cuda(), q, s)
+    rq, rs = O.quantize_act_1x128_ue8m0(x.float().numpy())
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
 @pytest.mark.parametrize("E,R,C", [(1, 128, 128), (3, 256, 384), (2, 2048, 1024)])
 def test_quantize_weight_bit_exact(E, R, C):
     rng = np.random.default_rng(E * R + C)

@@ -155,6 +155,42 @@ def test_quantize_act_properties():
             assert (err <= bound + 1e-30).all()
 
 
+def test_quantize_act_ue8m0_properties():
+    """Power-of-two scales: each group's scale is the smallest power of two
+    not below amax/448, so the group's largest code lands in [224, 448], the
+    reconstruction error is at most half an E4M3 spacing, and a group whose
+    amax/448 already is a power of two quantises exactly as with the plain
+    amax/448 scale."""
+    rng = np.random.default_rng(16)
+    x = bf16_round(rng.standard_normal((7, 512)).astype(np.float32))
+    x[2, 128:256] = 0.0                                 # an all-zero group
+    x[4, :128] = bf16_round(rng.uniform(-13.0, 13.0, 128).astype(np.float32))
+    x[4, 17] = 14.0                                     # amax/448 = 2^-5 exactly
+    q, s = moe.quantize_act_1x128_ue8m0(x)
+    assert q.shape == x.shape and s.shape == (7, 4)
+    assert s[2, 1] == 0 and (q[2, 128:256] == 0).all()
+    q0, s0 = moe.quantize_act_1x128(x)
+    assert s[4, 0] == np.float32(2.0 ** -5) and s0[4, 0] == s[4, 0]
+    assert np.array_equal(q[4, :128], q0[4, :128])
+    for m in range(7):
+        for g in range(4):
+            grp = x[m, 128 * g:128 * (g + 1)].astype(np.float64)
+            amax = np.abs(grp).max()
+            if amax == 0:
+                continue
+            sg = float(s[m, g])
+            frac, _ = np.frexp(sg)
+            assert frac == 0.5                                          # a power of two
+            base = float(np.float32(np.float32(amax) / np.float32(448)))
+            assert base <= sg < 2 * base or sg == base
+            top = np.abs(e4m3_decode(q[m, 128 * g:128 * (g + 1)])).max()
+            assert 224.0 <= top <= 448.0
+            deq = e4m3_decode(q[m, 128 * g:128 * (g + 1)]) * sg
+            err = np.abs(deq - grp)
+            bound = np.maximum(np.abs(grp) * 2.0 ** -4, 2.0 ** -10 * sg) * (1 + 1e-6)
+            assert (err <= bound + 1e-30).all()
+
+
 def test_quantize_weight_blocks_match_act_quantiser_on_blocks():
     """A 128x128 block quantises like one group of 16384 values."""
     rng = np.random.default_rng(7)
