@@ -221,7 +221,10 @@ typedef struct moe_fwd_args {
                                               after the gate/up kernel, after the down kernel
                                               and after the combine kernel (per-kernel
                                               timing; events between the launches keep them
-                                              from overlapping; no effect if NULL)           */
+                                              from overlapping; no effect if NULL).  On the
+                                              vector path the staging and combine intervals
+                                              are empty: its two kernels are timed as the
+                                              gate/up and down intervals                     */
   int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
 } moe_fwd_args;
 
