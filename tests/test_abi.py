@@ -66,6 +66,12 @@ def test_workspace_sizes(lib):
     small = moe_forward_workspace_size(8, 7168, 256, 257, 9, 64, 4608)
     assert 72 * 7168 * 2 + 4608 * 256 <= small < 72 * 7168 * 2 + 4608 * 256 + 4608 * 7168
     assert moe_forward_workspace_size(8, 7168, 256, 0, 9, 64, 4608) == 0
+    # sizes the vector path supports also hold its FP32 silu(gate) * up rows
+    # by route ([R, I] floats); one token more than it takes does not
+    at64 = moe_forward_workspace_size(64, 256, 256, 8, 2, 64, 64 * 2 + 8 * 63)
+    at65 = moe_forward_workspace_size(65, 256, 256, 8, 2, 64, 64 * 2 + 8 * 63)
+    # (65 tokens add two routes' rows elsewhere: 2 x 256 x 2 bytes, plus rounding)
+    assert 128 * 256 * 4 - 2048 <= at64 - at65 <= 128 * 256 * 4
     assert moe_plan_workspace_size(8192, 8, 288) >= 8192 * 8 * 4 + 288 * 4
 
 
