@@ -343,7 +343,7 @@ def expert_routes(topk_ids, E, tokens):
 
 def moe_forward(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
                 out_prior, routed_scale=1.0, tokens=None, return_inter=False,
-                round_bf16=True):
+                round_bf16=True, combine="fp32", workers=1):
     """Fused MoE expert forward, FP32 emulation ([FI-4287 summary]).
 
     a_q [M,H] uint8, a_s [M,H/128] f32, w13_q [E,2I,H] uint8 in the LOGICAL
@@ -357,7 +357,21 @@ def moe_forward(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
     {(t, j): (codes [I], scales [I/128])} of the requantised intermediate.
     Tokens are independent, so any subset gives exactly the rows a full run
     would give.
+
+    ``combine`` chooses how a token's route contributions c_j = y_j * w_j
+    reach ``out`` (reading 13):
+      "fp32"          acc = f32(prior); acc = f32(acc + c_j) in route order;
+                      out = bf16(acc): the parity target;
+      "bf16_route"    each c_j is first rounded to BF16, then summed as above
+                      (the tensor-core path's order of roundings);
+      "bf16_stepwise" acc = bf16(prior); acc = bf16(f32(acc) + c_j) after
+                      every route, the pages' BF16 reduce-add into ``out``;
+                      bounds the design space, not a parity target.
+    ``workers`` > 1 computes the experts' routes in that many threads (numpy
+    releases the interpreter lock in its kernels) and combines in the same
+    fixed order, so the output is bit-identical to ``workers=1``.
     """
+    assert combine in ("fp32", "bf16_route", "bf16_stepwise")
     M, H = a_q.shape
     E, N, _ = w13_q.shape
     I = N // 2
@@ -368,13 +382,23 @@ def moe_forward(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
     rs = np.float32(routed_scale)
     route_y = {}
     inter = {}
-    for e, (ts, js) in sorted(expert_routes(topk_ids, E, tokens).items()):
+
+    def expert_part(e, ts, js):
         acc = gemm1_expert(a_q[ts], a_s[ts], w13_q[e], w13_s[e])
         h = swiglu(acc, I)
         qi, si = requant_1x128(h)
         y = gemm2_expert(qi, si, w2_q[e], w2_s[e])
         wr = f32(f32(np.asarray(topk_w)[ts, js]) * rs)
-        y = f32(y * wr[:, None])
+        return ts, js, f32(y * wr[:, None]), qi, si
+
+    groups = sorted(expert_routes(topk_ids, E, tokens).items())
+    if workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=workers) as pool:
+            parts = list(pool.map(lambda g: expert_part(g[0], *g[1]), groups))
+    else:
+        parts = [expert_part(e, ts, js) for e, (ts, js) in groups]
+    for ts, js, y, qi, si in parts:
         for n, (t, j) in enumerate(zip(ts, js)):
             route_y[(int(t), int(j))] = y[n]
             if return_inter:
@@ -382,11 +406,16 @@ def moe_forward(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
     out = np.empty((tokens.size, H), dtype=np.float32)
     prior = f32(out_prior)
     for i, t in enumerate(tokens):
-        acc = prior[t].copy()
+        acc = bf16_round(prior[t]) if combine == "bf16_stepwise" else prior[t].copy()
         for j in range(k):
             y = route_y.get((int(t), j))
-            if y is not None:
-                acc = f32(acc + y)
+            if y is None:
+                continue
+            if combine == "bf16_route":
+                y = bf16_round(y)
+            acc = f32(acc + y)
+            if combine == "bf16_stepwise":
+                acc = bf16_round(acc)
         out[i] = bf16_round(acc) if round_bf16 else acc
     if return_inter:
         return out, inter

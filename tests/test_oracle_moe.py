@@ -411,3 +411,62 @@ def test_forward_token_subset_equals_full_rows():
     full = moe.moe_forward(**p)
     sub = moe.moe_forward(**p, tokens=[4, 1])
     assert np.array_equal(sub, full[[4, 1]])
+
+
+def test_forward_expert_partitioned_is_bit_identical():
+    """Experts computed in several threads, combined in the same fixed order,
+    give exactly the single-threaded output and intermediate."""
+    p = _tiny_problem(22, M=6, E=5, k=3, masked=((1, 2),))
+    a, ia = moe.moe_forward(**p, return_inter=True)
+    b, ib = moe.moe_forward(**p, return_inter=True, workers=3)
+    assert np.array_equal(a, b)
+    assert ia.keys() == ib.keys()
+    for key in ia:
+        assert np.array_equal(ia[key][0], ib[key][0]) and np.array_equal(ia[key][1], ib[key][1])
+
+
+def _route_contributions(p):
+    """c[j] [M, H]: route j's weighted down projection alone (other routes
+    masked, zero prior; with one route the FP32 accumulator is c_j exactly)."""
+    k = p["topk_ids"].shape[1]
+    zero = np.zeros_like(p["out_prior"])
+    out = []
+    for j in range(k):
+        ids = np.full_like(p["topk_ids"], -1)
+        ids[:, j] = p["topk_ids"][:, j]
+        out.append(moe.moe_forward(**dict(p, topk_ids=ids, out_prior=zero), round_bf16=False).astype(np.float64))
+    return out
+
+
+def test_forward_combine_modes():
+    """The three ways route contributions reach `out` agree exactly for one
+    route onto a zero prior (a single rounding each way), and otherwise stay
+    within the bounds their extra BF16 roundings allow: half a BF16 ulp
+    (2^-8 relative: 7 stored mantissa bits) per rounded contribution for
+    per-route rounding, and per step of the running sum for the stepwise
+    reduce-add."""
+    one = _tiny_problem(23, M=3, E=3, k=1)
+    one["out_prior"] = np.zeros_like(one["out_prior"])
+    ref = moe.moe_forward(**one)
+    for mode in ("bf16_route", "bf16_stepwise"):
+        assert np.array_equal(moe.moe_forward(**one, combine=mode), ref)
+
+    p = _tiny_problem(24, M=4, E=4, k=3)
+    c = _route_contributions(p)
+    prior = p["out_prior"].astype(np.float64)
+    acc = moe.moe_forward(**p, round_bf16=False).astype(np.float64)
+    slack = 1e-5 * (np.abs(prior) + sum(np.abs(cj) for cj in c)) + 1e-30
+    # per-route rounding: every contribution moves by at most 2^-8 of itself
+    route = moe.moe_forward(**p, combine="bf16_route", round_bf16=False).astype(np.float64)
+    assert (np.abs(route - acc) <= 2.0 ** -8 * sum(np.abs(cj) for cj in c) + slack).all()
+    # stepwise: the prior and each running sum are rounded once more
+    step = moe.moe_forward(**p, combine="bf16_stepwise").astype(np.float64)
+    running = [np.abs(prior)]
+    s = prior.copy()
+    for cj in c:
+        s = s + cj
+        running.append(np.abs(s))
+    bound = 2.0 ** -8 * sum(running) * (1 + 2.0 ** -7) + slack
+    assert (np.abs(step - acc) <= bound).all()
+    # and the modes do differ somewhere on this problem
+    assert not np.array_equal(moe.moe_forward(**p, combine="bf16_stepwise"), moe.moe_forward(**p))
