@@ -114,6 +114,39 @@ def test_forward_small_each_path(name, mode):
     assert int(prob.status.item()) == 0
 
 
+def _bf16_ulps(a, b):
+    """Distance in BF16 steps between two float32 arrays holding BF16 values."""
+    def ordered(x):
+        bits = (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.int64)
+        return np.where(bits & 0x8000, 0x8000 - bits, bits)   # monotone in the value
+    return np.abs(ordered(a) - ordered(b))
+
+
+TIGHT = [(n, L.TILE_SINGLE) for n in SMALL] + [(n, L.TILE_VECTOR) for n in VECTOR_SMALL]
+
+
+@pytest.mark.parametrize("name,mode", TIGHT, ids=[f"{n}-{'tiles' if m == L.TILE_SINGLE else 'vector'}" for n, m in TIGHT])
+def test_forward_matches_oracle_in_its_rounding_order(name, mode):
+    """With the oracle adding the route contributions in the path's own order
+    of roundings (each contribution rounded to BF16 first for the tensor-core
+    tiles, reading 13; plain FP32 for the vector path, reading 27), the
+    outputs agree bit for bit apart from rare near-ties: at most 0.1% of the
+    elements differ, none by more than one BF16 step at the output's largest
+    magnitude (a tie in one contribution's own rounding can be several steps
+    of an element where the routes nearly cancel)."""
+    prob = DeviceProblem(SMALL[name])
+    _run(prob, debug=False, tile_mode=mode)
+    cfg = prob.cfg
+    inp, _ = oracle_inputs(cfg, prob.routing, np.arange(cfg.M))
+    combine = "bf16_route" if mode == L.TILE_SINGLE else "fp32"
+    ref = O.moe_forward(**inp, routed_scale=cfg.routed_scale, combine=combine)
+    got = prob.out.float().cpu().numpy()
+    ulps = _bf16_ulps(got, ref)
+    print(f"{name} {combine}: {int((ulps > 0).sum())} of {ulps.size} differ, max {int(ulps.max())} step")
+    assert (ulps > 0).sum() <= max(2, 0.001 * ulps.size)
+    assert np.abs(got.astype(np.float64) - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
 # ------------------------------------------------------------------ full-size workloads, sampled tokens
 
 FULL = {
