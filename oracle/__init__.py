@@ -17,7 +17,8 @@ Sources (pages, cited by title and section throughout):
 * sglang-glm53-flash-sm120 pull request #13, "SM120 FP8 prefill" --
   description and validation notes.
 * The E4M3 format itself is defined by the OCP 8-bit floating point
-  specification (OFP8); the pages only name it.
+  specification (OFP8), E2M1 by the OCP Microscaling Formats (MX)
+  specification; the pages only name them.
 
 Modules:
 
@@ -29,6 +30,9 @@ Modules:
   generator, and the parity metrics (tolerances of the forward).
 * ``router`` -- top-k expert selection and route weights from router logits
   (the reading of the companion router the pages name).
+* ``w4a8`` -- the E2M1-K32 weight x per-row FP8 activation variant of the
+  expert computation (E2M1 codec, K32 and per-row quantisers, the forward and
+  an FP64 twin used to pin it).
 
 Pinning status: every function here is pinned by a CPU test under
 ``tests/`` (exhaustive codec checks, closed forms, brute force on tiny inputs,
