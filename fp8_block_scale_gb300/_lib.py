@@ -65,6 +65,37 @@ class MoeFwdArgs(ctypes.Structure):
 TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_VECTOR = 0, 1, 2, 3
 
 
+class MoeW4A8Args(ctypes.Structure):
+    """Mirror of ``struct moe_w4a8_args`` (include/moe_w4a8.h)."""
+    _fields_ = [
+        ("a", ctypes.c_void_p),
+        ("a_scale", ctypes.c_void_p),
+        ("w13", ctypes.c_void_p),
+        ("w13_scale", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p),
+        ("topk_weights", ctypes.c_void_p),
+        ("sorted_token_ids", ctypes.c_void_p),
+        ("expert_ids", ctypes.c_void_p),
+        ("num_tokens_post_padded", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("device_status", ctypes.c_void_p),
+        ("debug_q_inter", ctypes.c_void_p),
+        ("debug_s_inter", ctypes.c_void_p),
+        ("M", ctypes.c_int64),
+        ("sorted_cap", ctypes.c_int64),
+        ("blocks_cap", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("H", ctypes.c_int32),
+        ("I", ctypes.c_int32),
+        ("E", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
+        ("block_m", ctypes.c_int32),
+        ("routed_scale", ctypes.c_float),
+    ]
+
+
 _lib = None
 
 _SIGS = {
@@ -94,6 +125,12 @@ _SIGS = {
     "moe_fp8_block_scale_forward": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
     "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "moe_fp8_block_scale_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
+    "moe_quantize_act_per_row": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_quantize_weight_k32": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_w4a8_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "moe_w4a8_forward": (ctypes.c_int, [ctypes.POINTER(MoeW4A8Args), ctypes.c_void_p]),
 }
 
 
@@ -259,3 +296,55 @@ def moe_fp8_block_scale_forward_noalloc(args, stream=None):
     """Forward without a caller workspace (static device scratch; see the header)."""
     _check("moe_fp8_block_scale_forward_noalloc",
            load().moe_fp8_block_scale_forward_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+# ---------------------------------------------------------------- E2M1-K32 weights x FP8 activations
+
+def moe_quantize_act_per_row(x_bf16, q, scale, stream=None):
+    M, K = x_bf16.shape
+    _check("moe_quantize_act_per_row", load().moe_quantize_act_per_row(
+        _ptr(x_bf16), M, K, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_weight_k32(w_bf16, q_packed, scale, stream=None):
+    """w_bf16 [..., K] (leading dimensions folded into rows) -> q_packed [..., K/2], scale [..., K/32]."""
+    K = w_bf16.shape[-1]
+    _check("moe_quantize_weight_k32", load().moe_quantize_weight_k32(
+        _ptr(w_bf16), w_bf16.numel() // K, K, _ptr(q_packed), _ptr(scale), _stream(stream)))
+
+
+def moe_w4a8_workspace_size(M, H, I, top_k):
+    return load().moe_w4a8_workspace_size(M, H, I, top_k)
+
+
+def make_w4a8_args(a, a_scale, w13, w13_scale, w2, w2_scale, topk_weights, sorted_token_ids, expert_ids,
+                   num_tokens_post_padded, out, workspace, top_k, block_m, routed_scale=1.0,
+                   device_status=None, debug_q_inter=None, debug_s_inter=None):
+    """Fill a ``moe_w4a8_args`` from tensors; w13 is [E, 2I, H/2] packed codes."""
+    M, H = a.shape
+    E, N, _ = w13.shape
+    args = MoeW4A8Args()
+    args.a, args.a_scale = a.data_ptr(), a_scale.data_ptr()
+    args.w13, args.w13_scale = w13.data_ptr(), w13_scale.data_ptr()
+    args.w2, args.w2_scale = w2.data_ptr(), w2_scale.data_ptr()
+    args.topk_weights = topk_weights.data_ptr()
+    args.sorted_token_ids = sorted_token_ids.data_ptr()
+    args.expert_ids = expert_ids.data_ptr()
+    args.num_tokens_post_padded = num_tokens_post_padded.data_ptr()
+    args.out = out.data_ptr()
+    args.workspace = workspace.data_ptr()
+    args.device_status = device_status.data_ptr() if device_status is not None else None
+    args.debug_q_inter = debug_q_inter.data_ptr() if debug_q_inter is not None else None
+    args.debug_s_inter = debug_s_inter.data_ptr() if debug_s_inter is not None else None
+    args.M = M
+    args.sorted_cap = sorted_token_ids.numel()
+    args.blocks_cap = expert_ids.numel()
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    args.H, args.I, args.E = H, N // 2, E
+    args.top_k, args.block_m = top_k, block_m
+    args.routed_scale = routed_scale
+    return args
+
+
+def moe_w4a8_forward(args, stream=None):
+    _check("moe_w4a8_forward", load().moe_w4a8_forward(ctypes.byref(args), _stream(stream)))

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_fp8.so")
-SOURCES = ["api.cu", "plan.cu", "prep.cu", "forward.cu", "vector.cu", "noalloc.cu", "router.cu"]
+SOURCES = ["api.cu", "plan.cu", "prep.cu", "forward.cu", "vector.cu", "noalloc.cu", "router.cu", "w4a8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]
@@ -40,7 +40,8 @@ def build(verbose=False, force=False):
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".cuh", ".h"))]
-    headers.append(os.path.join(ROOT, "include", "moe_fp8.h"))
+    inc = os.path.join(ROOT, "include")
+    headers += [os.path.join(inc, h) for h in os.listdir(inc) if h.endswith(".h")]
     objs = []
     jobs = []
     for src in SOURCES:

@@ -11,6 +11,7 @@ import torch
 
 from fp8_block_scale_gb300 import workloads as W
 from . import moe as O
+from . import w4a8 as OW
 from .numerics import e4m3_decode
 
 # The numerical acceptance bar of the forward: relative L2 error of `out`,
@@ -53,6 +54,37 @@ def oracle_inputs(cfg, routing, tokens, device=None):
         N, H, I = cfg.N, cfg.H, cfg.I
         w13_q, w13_s = [np.zeros((N, H), np.uint8)], [np.zeros((N // 128, H // 128), np.float32)]
         w2_q, w2_s = [np.zeros((H, I), np.uint8)], [np.zeros((H // 128, I // 128), np.float32)]
+    prior = W.make_out_prior(cfg, device=device)[torch.as_tensor(tokens, device=device)].float().cpu().numpy()
+    inp = dict(a_q=a_q, a_s=a_s, w13_q=np.stack(w13_q), w13_s=np.stack(w13_s), w2_q=np.stack(w2_q),
+               w2_s=np.stack(w2_s), topk_ids=ids_c, topk_w=routing.topk_weights.numpy()[tokens], out_prior=prior)
+    return inp, experts
+
+
+def oracle_inputs_w4a8(cfg, routing, tokens, device=None):
+    """Oracle inputs of the E2M1-K32 x FP8 forward for `tokens` (oracle.w4a8),
+    from the same raw values as ``oracle_inputs``: a compact problem over the
+    experts the tokens touch, weights as unpacked E2M1 codes."""
+    if device is None:
+        device = "cuda" if torch.cuda.is_available() else "cpu"
+    tokens = np.asarray(tokens, dtype=np.int64)
+    ids = routing.topk_ids.to(torch.int64).numpy()[tokens]
+    experts = sorted({int(e) for e in ids.reshape(-1) if 0 <= e < cfg.E})
+    remap = {e: i for i, e in enumerate(experts)}
+    ids_c = np.array([[remap.get(int(e), -1) for e in row] for row in ids], dtype=np.int64)
+    x = W.make_activations(cfg, device=device)[torch.as_tensor(tokens, device=device)].float().cpu().numpy()
+    a_q, a_s = OW.quantize_act_per_row(x)
+    w13_q, w13_s, w2_q, w2_s = [], [], [], []
+    for e in experts:
+        q, s = OW.quantize_weight_k32(W.make_expert_weights(cfg, e, "w13", device).float().cpu().numpy())
+        q2, s2 = OW.quantize_weight_k32(W.make_expert_weights(cfg, e, "w2", device).float().cpu().numpy())
+        if e in routing.zero_scale_experts:
+            s[:] = 0
+            s2[:] = 0
+        w13_q.append(q); w13_s.append(s); w2_q.append(q2); w2_s.append(s2)
+    if not experts:
+        N, H, I = cfg.N, cfg.H, cfg.I
+        w13_q, w13_s = [np.zeros((N, H), np.uint8)], [np.zeros((N, H // 32), np.float32)]
+        w2_q, w2_s = [np.zeros((H, I), np.uint8)], [np.zeros((H, I // 32), np.float32)]
     prior = W.make_out_prior(cfg, device=device)[torch.as_tensor(tokens, device=device)].float().cpu().numpy()
     inp = dict(a_q=a_q, a_s=a_s, w13_q=np.stack(w13_q), w13_s=np.stack(w13_s), w2_q=np.stack(w2_q),
                w2_s=np.stack(w2_s), topk_ids=ids_c, topk_w=routing.topk_weights.numpy()[tokens], out_prior=prior)

@@ -157,3 +157,64 @@ def test_router_host_validation_without_gpu(lib):
     assert f(p, 0, -1, 8, 2, 1.0, 1, p, 32, p, None) == 2         # negative M
     assert f(None, 0, 4, 8, 2, 1.0, 1, p, 32, p, None) == 1       # null logits
     assert f(None, 0, 0, 8, 2, 1.0, 1, None, 32, None, None) == 0  # nothing to do
+
+
+def test_w4a8_host_validation_without_gpu(lib):
+    """moe_w4a8_forward and its quantisers reject bad arguments on the host."""
+    from fp8_block_scale_gb300._lib import MoeW4A8Args
+    f = lib.moe_w4a8_forward
+    assert f(None, None) == 1                                    # MOE_ERR_NULL
+    a = MoeW4A8Args()
+    a.M, a.H, a.I, a.E, a.top_k, a.block_m = 4, 256, 128, 8, 2, 16
+    a.sorted_cap, a.blocks_cap = 160, 10
+    a.routed_scale = 1.0
+    for field, bad in (("H", 240), ("H", 0), ("I", 48), ("I", 16), ("top_k", 65), ("top_k", 0), ("E", 0),
+                       ("block_m", 12), ("block_m", 72), ("block_m", 0), ("M", -1)):
+        good = getattr(a, field)
+        setattr(a, field, bad)
+        assert f(ctypes.byref(a), None) == 2, (field, bad)     # MOE_ERR_SHAPE
+        setattr(a, field, good)
+    a.block_m, a.H = 64, 4096
+    assert f(ctypes.byref(a), None) == 2                         # block_m * H above 128 KiB
+    a.block_m, a.H = 16, 256
+    a.sorted_cap = 159
+    assert f(ctypes.byref(a), None) == 4                         # capacity
+    a.sorted_cap = 160
+    assert f(ctypes.byref(a), None) == 1                         # null pointers
+    for name in ("a", "a_scale", "w13", "w13_scale", "w2", "w2_scale", "topk_weights", "sorted_token_ids",
+                 "expert_ids", "num_tokens_post_padded", "out", "workspace"):
+        setattr(a, name, 4096)
+    a.debug_q_inter = 4096
+    assert f(ctypes.byref(a), None) == 1                         # debug codes without their scales
+    a.debug_q_inter = None
+    a.w2 = 4100
+    assert f(ctypes.byref(a), None) == 3                         # misaligned
+    a.w2 = 4096
+    a.workspace_bytes = lib.moe_w4a8_workspace_size(4, 256, 128, 2) - 1
+    assert f(ctypes.byref(a), None) == 4                         # workspace too small
+    a.M = 0
+    assert f(ctypes.byref(a), None) == 0                         # nothing to do
+
+    p = _fake(4096)
+    assert lib.moe_quantize_act_per_row(p, 4, 100, p, p, None) == 2
+    assert lib.moe_quantize_act_per_row(p, -1, 128, p, p, None) == 2
+    assert lib.moe_quantize_act_per_row(None, 4, 128, p, p, None) == 1
+    assert lib.moe_quantize_act_per_row(_fake(4097), 4, 128, p, p, None) == 3
+    assert lib.moe_quantize_act_per_row(None, 0, 128, None, None, None) == 0
+    assert lib.moe_quantize_weight_k32(p, 4, 48, p, p, None) == 2
+    assert lib.moe_quantize_weight_k32(p, 0, 64, p, p, None) == 2
+    assert lib.moe_quantize_weight_k32(None, 4, 64, p, p, None) == 1
+    assert lib.moe_quantize_weight_k32(p, 4, 64, _fake(4104), p, None) == 3
+
+
+def test_w4a8_workspace_size(lib):
+    """Route flags, SwiGLU rows (FP32), their codes, row scales and the FP32
+    route contributions, each region rounded up to 256 bytes."""
+    def r256(n):
+        return -(-n // 256) * 256
+    for M, H, I, k in ((3, 256, 128, 2), (1, 4096, 1024, 8), (37, 384, 96, 3), (0, 256, 128, 2)):
+        R = M * k
+        want = r256(4 * R) + r256(4 * R * I) + r256(R * I) + r256(4 * R) + r256(4 * R * H)
+        assert lib.moe_w4a8_workspace_size(M, H, I, k) == want
+    assert lib.moe_w4a8_workspace_size(-1, 256, 128, 2) == 0
+    assert lib.moe_w4a8_workspace_size(4, 256, 128, 0) == 0
