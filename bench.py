@@ -651,7 +651,50 @@ def extra_sweep(cfg, prob, flush, peaks):
     for label, (M, E, k) in (("router_m1", (1, 257, 9)), ("router_m8192", (8192, 288, 8))):
         out[label] = measure_router(M, E, k, flush, peaks)
     torch.cuda.empty_cache()
+    for M in (1, 1024):
+        try:  # the E2M1-K32 path's timing must not hide the rest of the sweep
+            out[f"w4a8_e288_m{M}"] = measure_w4a8(M, flush, peaks)
+        except Exception as ex:
+            out[f"w4a8_e288_m{M}"] = {"error": str(ex)}
+        torch.cuda.empty_cache()
     return out
+
+
+def measure_w4a8(M, flush, peaks, steps=5, warmup=3):
+    """moe_w4a8_forward (E2M1-K32 weights x per-row FP8 activations, the
+    CUDA-core path) at the SM120 page's timing shape E288/H4096/I1024/top-8
+    with plan blocks of 16 rows; the plan is built once and L2 is flushed
+    before each timed forward.  FLOP = Rv * 6 * H * I; bytes = the touched
+    experts' packed codes and K32 scales (1.875 * H * I each) + activations,
+    their row scales and `out` read and written."""
+    import torch
+    from fp8_block_scale_gb300 import workloads as W
+    from fp8_block_scale_gb300.problem import W4A8Problem
+    cfg = W.MoEConfig(f"w4a8_e288_m{M}", M=M, H=4096, I=1024, E=288, top_k=8, block_m=16)
+    p = W4A8Problem(cfg)
+    p.run_plan()
+    args = p.fwd_args()
+    for _ in range(warmup):
+        p.run_forward(args)
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        p.run_forward(args)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    ids = p.routing.topk_ids.to(torch.int64)
+    valid = ids[(ids >= 0) & (ids < cfg.E)]
+    Rv, U = int(valid.numel()), int(torch.unique(valid).numel())
+    flop = Rv * 6 * cfg.H * cfg.I
+    nbytes = U * 1.875 * cfg.H * cfg.I + M * (cfg.H + 4) + 4 * M * cfg.H
+    return {"M": M, "ms_forward": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "path": "CUDA cores (gate/up, requant, down, combine kernels and a flag memset)"}
 
 
 def measure_router(M, E, k, flush, peaks, steps=20, warmup=5):
@@ -693,9 +736,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing (profiling runs)")
     ap.add_argument("--oracle-child", nargs=2, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--w4a8", action="store_true",
+                    help="time only the E2M1-K32 weight path at 1 and 1024 tokens (one JSON line)")
     args = ap.parse_args()
     if args.oracle_child:
         _oracle_child(*args.oracle_child)
+        return
+    if args.w4a8:
+        import torch
+        from fp8_block_scale_gb300 import _lib as L
+        L.load()
+        peaks = load_peaks()
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        print(json.dumps({f"w4a8_e288_m{M}": measure_w4a8(M, flush, peaks) for M in (1, 1024)}), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3
