@@ -3,7 +3,8 @@
 // description): E2M1 weight codes with one FP32 scale per 32 elements of K,
 // applied in FP32, and E4M3 activations with one FP32 scale per row.
 //
-// The projections run on the CUDA cores, one plan block per CTA:
+// The projections run on the CUDA cores; each CTA of the first three kernels
+// takes one plan block (in the projections, and a group of columns):
 //   w4a8_up_kernel       gate/up rows of the block's expert against the block's
 //                        activation rows (staged in shared memory), SwiGLU;
 //   w4a8_requant_kernel  each route's SwiGLU row requantised to E4M3 with one
@@ -12,9 +13,10 @@
 //                        weight: one FP32 contribution row per route;
 //   w4a8_combine_kernel  each token's contributions added in slot order onto
 //                        f32(out), rounded once to BF16.
-// In the two projections a lane takes 32-wide K blocks (lane, lane + 32, ...):
-// one 16-byte load of packed weight codes and one scale per block, the codes
-// decoded once and applied to up to kRowChunk rows held in registers.
+// In the two projections a warp takes a column and its lanes the 32-wide K
+// blocks (lane, lane + 32, ...): one 16-byte load of packed weight codes and
+// one scale per block, the codes decoded once per chunk of kRowChunk rows,
+// whose partial sums stay in registers until a warp reduction.
 #include "common.cuh"
 #include "../../include/moe_w4a8.h"
 
