@@ -4,7 +4,8 @@ As for the block-FP8 oracle, nothing here compares the oracle with itself:
 the codec against the format's value table and a brute-force nearest-value
 search, the dot products against integer arithmetic, the quantisers and the
 GEMM against invariants and special cases that reduce to torch routines, the
-forward against an independently written float64 twin.
+forward against an independently written float64 twin and against the
+block-FP8 oracle where the two formats describe the same numbers.
 """
 
 import numpy as np
@@ -297,3 +298,43 @@ def test_forward_routed_scale_is_a_route_weight_factor():
     a = w4a8.moe_forward_w4a8(**p, routed_scale=2.0, round_bf16=False)
     b = w4a8.moe_forward_w4a8(**dict(p, topk_w=f32(p["topk_w"] * 2)), round_bf16=False)
     np.testing.assert_array_equal(a, b)
+
+
+def test_forward_equals_block_fp8_forward_when_formats_coincide():
+    """E2M1 values are E4M3 values, so weights whose K32 scales are constant
+    over each 128x128 block, activations whose row scale is every group's
+    scale, and I = 128 (one requant group per row) describe the same real
+    numbers to both oracles.  They agree to FP32 accuracy despite different
+    code: 32-wide against 128-wide blocks, the activation scale applied
+    after the sum against inside each promotion."""
+    from oracle import moe
+    rng = np.random.default_rng(27)
+    M, H, I, E, k = 5, 256, 128, 3, 2
+    N = 2 * I
+    aq = e4m3_encode((rng.standard_normal((M, H)) * 30).astype(np.float32))
+    as_row = (rng.random(M) + 0.5).astype(np.float32)
+    w13c = rng.integers(0, 16, size=(E, N, H)).astype(np.uint8)
+    w2c = rng.integers(0, 16, size=(E, H, I)).astype(np.uint8)
+    s13 = (rng.random((E, N // 128, H // 128)) * 0.01 + 0.001).astype(np.float32)
+    s2 = (rng.random((E, H // 128, I // 128)) * 0.01 + 0.001).astype(np.float32)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int64)
+    tw = rng.random((M, k)).astype(np.float32)
+    prior = bf16_round((rng.standard_normal((M, H)) * 0.1).astype(np.float32))
+
+    def k32(s):          # [E, R/128, C/128] -> one K32 scale per row and 32 columns
+        return np.repeat(np.repeat(s, 128, axis=1), 4, axis=2)
+
+    out4, inter4 = w4a8.moe_forward_w4a8(aq, as_row, w13c, k32(s13), w2c, k32(s2), ids, tw, prior,
+                                         routed_scale=1.5, return_inter=True, round_bf16=False)
+    out8, inter8 = moe.moe_forward(aq, np.repeat(as_row[:, None], H // 128, axis=1),
+                                   e4m3_encode(w4a8.e2m1_decode(w13c)), s13,
+                                   e4m3_encode(w4a8.e2m1_decode(w2c)), s2, ids, tw, prior,
+                                   routed_scale=1.5, return_inter=True, round_bf16=False)
+    n_diff = 0
+    for key, (codes, scale) in inter4.items():
+        c8, s8 = inter8[key]
+        n_diff += int((codes != c8).sum())
+        np.testing.assert_allclose(scale, s8[0], rtol=1e-6)
+    assert n_diff <= 2
+    rel = np.linalg.norm(out4.astype(np.float64) - out8) / np.linalg.norm(out8.astype(np.float64) - prior)
+    assert rel < 1e-5, rel
