@@ -483,6 +483,23 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# A rank that dies between steps must not hold the other ranks (and their
+# GPUs) in their next collective for the backends' default timeouts (10 to
+# 30 minutes): the process group gives up after this long, far above the
+# longest gap between two collectives of a healthy run (problem set-up plus
+# the timed steps).
+PG_TIMEOUT_S = 300
+
+
+def init_distributed(backend, timeout_s=PG_TIMEOUT_S):
+    """Join the process group of a torchrun launch (env:// rendezvous) with a
+    bounded collective timeout; returns the torch.distributed module."""
+    import datetime
+    import torch.distributed as tdist
+    tdist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
+    return tdist
+
+
 def max_over_ranks(x, dist, device):
     """The maximum of x over all ranks (x itself when not distributed).  A NaN
     on any rank (a failed measurement) makes the result NaN: a MAX reduction
@@ -756,14 +773,12 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     dist = None
     if world > 1:
-        import torch.distributed as tdist
         if args.impl == "ours":
             import torch
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-            tdist.init_process_group("nccl")
+            dist = init_distributed("nccl")
         else:
-            tdist.init_process_group("gloo")
-        dist = tdist
+            dist = init_distributed("gloo")
     try:
         if args.impl == "reference":
             run_reference(args, rank)

@@ -50,6 +50,51 @@ def test_max_over_ranks_and_job_throughput_with_two_gloo_ranks(tmp_path):
         assert r["e2e_nan"]                       # a failed measurement on one rank is not hidden
 
 
+def _dead_rank_main(rank, world, port, out_path, mode="exit"):
+    """Rank 1 leaves between steps (no kernel or collective in flight): it
+    exits ("exit"), or stays alive without joining the next collective
+    ("stall").  Rank 0 must learn of it in its next collective, with an
+    error, not a hang: at once when the peer's connection closes, after the
+    process group's timeout when the peer is silent."""
+    import time
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    os.environ["RANK"], os.environ["WORLD_SIZE"] = str(rank), str(world)
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.init_distributed("gloo", timeout_s=5)
+    d.barrier()                                   # one healthy step together
+    if rank == 1:
+        if mode == "stall":
+            time.sleep(9)                         # alive, but never reaches the collective
+        os._exit(0)                               # the rank is gone; nothing of it is in flight
+    t0 = time.monotonic()
+    try:
+        bench.max_over_ranks(1.0, d, "cpu")
+        outcome = "returned"
+    except Exception as ex:                       # the survivor's next collective fails
+        outcome = type(ex).__name__
+    with open(f"{out_path}.0", "w") as f:
+        json.dump({"outcome": outcome, "seconds": time.monotonic() - t0}, f)
+    os._exit(0)                                   # no clean shutdown with a dead peer
+
+
+@pytest.mark.parametrize("mode,limit_s", [("exit", 4.0), ("stall", 8.5)])
+def test_a_dead_rank_ends_the_survivors_next_collective_with_an_error(tmp_path, mode, limit_s):
+    port = _free_port()
+    out = str(tmp_path / "d")
+    mp.spawn(_dead_rank_main, args=(2, port, out, mode), nprocs=2, join=True)
+    res = json.load(open(f"{out}.0"))
+    assert res["outcome"] != "returned"
+    assert res["seconds"] < limit_s                # the 5 s timeout, not the backend's default
+
+
+def test_process_group_timeout_is_bounded():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert 60 <= bench.PG_TIMEOUT_S <= 600
+
+
 def test_single_process_helpers():
     sys.path.insert(0, ROOT)
     import bench
