@@ -41,7 +41,7 @@ typedef enum {
   MOE_ERR_ALIGN = 3,    /* a pointer is not 16-byte aligned                   */
   MOE_ERR_CAPACITY = 4, /* plan or workspace buffers too small                */
   MOE_ERR_DTYPE = 5,    /* unsupported id width                               */
-  MOE_ERR_DEVICE = 6,   /* pointer not on the current device / not sm_100+    */
+  MOE_ERR_DEVICE = 6,   /* pointer not on the current device / not sm_103     */
   MOE_ERR_CUDA = 7,     /* a CUDA runtime/driver call failed                  */
   MOE_ERR_TIMEOUT = 8   /* reserved for host-visible timeouts                 */
 } moe_status;
@@ -280,7 +280,8 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_strea
 /* Run the forward.  Constraints: H % 128 == 0; I % 128 == 0 (so 2I % 256 ==
  * 0); 1 <= top_k <= 64; 8 <= block_m <= 128, block_m % 8 == 0; sorted_cap >= blocks_cap *
  * block_m; blocks_cap >= 1; a, w13, w2 and the workspace 16-byte aligned; all
- * pointers on the current device, which must be sm_100 class or newer. */
+ * pointers on the current device, which must be sm_103 (GB300: the library
+ * is built for sm_103a only). */
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
