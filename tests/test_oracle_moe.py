@@ -97,6 +97,12 @@ def test_plan_capacity_is_tight():
     ids = np.arange(8).reshape(4, 2)
     _, _, P = moe.moe_plan(ids, E, bm)
     assert P == moe.plan_capacity(M, k, E, bm)[0] == 8 * 64
+    # more experts than routes: at most R experts are non-empty, so the bound
+    # is R * block_m (a decode step, 9 routes over 257 experts), and a step
+    # whose routes all go to different experts attains it
+    assert moe.plan_capacity(1, 9, 257, 64) == (9 * 64, 9)
+    _, b, P = moe.moe_plan(np.arange(0, 257, 29)[None, :9], 257, 64)
+    assert P == 9 * 64 and b.size == 9
 
 
 def test_plan_all_masked_is_empty():
@@ -135,9 +141,11 @@ def test_quantize_act_properties():
     rng = np.random.default_rng(6)
     x = bf16_round(rng.standard_normal((9, 384)).astype(np.float32))
     x[3, 128:256] = 0.0                                # an all-zero group
+    x[5, 0:128] = -0.0                                 # and one of negative zeros
     q, s = moe.quantize_act_1x128(x)
     assert q.shape == x.shape and s.shape == (9, 3)
     assert s[3, 1] == 0 and (q[3, 128:256] == 0).all()
+    assert s[5, 0] == 0 and (q[5, 0:128] == 0).all()  # scale 0 gives code 0x00, not -0 (0x80)
     deq = e4m3_decode(q) * np.repeat(s.astype(np.float64), 128, axis=1)
     for m in range(9):
         for g in range(3):

@@ -88,8 +88,10 @@ def test_quantize_weight_k32_properties():
     rng = np.random.default_rng(3)
     w = bf16_round((rng.standard_normal((2, 5, 128)) * 0.05).astype(np.float32))
     w[0, 1, 32:64] = 0.0                                    # one all-zero block
+    w[0, 2, 0:32] = -0.0                                    # one block of negative zeros
     w[1, 2, 96:128] *= 1000.0                               # one block far larger than the rest
     codes, scale = w4a8.quantize_weight_k32(w)
+    assert scale[0, 2, 0] == 0 and not codes[0, 2, 0:32].any()   # code 0, not -0 (8)
     assert codes.shape == w.shape and scale.shape == (2, 5, 4) and scale.dtype == np.float32
     assert scale[0, 1, 1] == 0 and not codes[0, 1, 32:64].any()
     g = w.reshape(2, 5, 4, 32)
@@ -119,9 +121,11 @@ def test_quantize_act_per_row_properties():
     rng = np.random.default_rng(4)
     x = bf16_round(rng.standard_normal((6, 256)).astype(np.float32) * np.array([1, 1e-3, 1e3, 1, 1, 1])[:, None])
     x[4] = 0.0
+    x[5] = -0.0
     codes, scale = w4a8.quantize_act_per_row(x)
     assert scale.shape == (6,) and scale[4] == 0 and not codes[4].any()
-    for t in (0, 1, 2, 3, 5):
+    assert scale[5] == 0 and not codes[5].any()             # code 0x00, not -0 (0x80)
+    for t in (0, 1, 2, 3):
         i = int(np.argmax(np.abs(x[t])))
         assert codes[t, i] & 0x7F == 0x7E                  # 448, the largest finite E4M3 magnitude
         assert (codes[t, i] >> 7) == int(np.signbit(x[t, i]))
