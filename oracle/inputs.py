@@ -104,6 +104,16 @@ def out_metrics(got, ref, prior=None):
     return res
 
 
+def bf16_ulps(a, b):
+    """Distance in BF16 steps between two float32 arrays holding BF16 values:
+    the bit patterns mapped to integers that increase with the value (+0 and
+    -0 coincide), then subtracted."""
+    def ordered(x):
+        bits = (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.int64)
+        return np.where(bits & 0x8000, 0x8000 - bits, bits)
+    return np.abs(ordered(a) - ordered(b))
+
+
 def code_diffs(got_codes, ref_codes):
     """(number of differing codes, number of differences that are not to an
     adjacent E4M3 value).  +0 and -0 count as equal."""

@@ -1,7 +1,8 @@
 """Planted-mistake check of the oracle's CPU pins (not collected by pytest).
 
-Each entry below is a plausible mistake in the oracle: a dropped term, a
-wrong sign, index or axis, a swapped operand, a wrong constant or tie rule.
+Each entry below is a plausible mistake in the oracle or in the parity
+metrics the GPU tests use: a dropped term, a wrong sign, index or axis, a
+swapped operand, a wrong constant or tie rule.
 The script copies ``oracle/`` and ``tests/`` into a temporary directory,
 plants one mistake at a time in the copy and runs the oracle pin tests
 there; every mistake must make at least one pin fail.  The repository is
@@ -22,11 +23,23 @@ import sys
 import tempfile
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_TESTS = ["tests/test_oracle_numerics.py", "tests/test_oracle_moe.py", "tests/test_oracle_router.py",
-             "tests/test_oracle_w4a8.py"]
+PIN_TESTS = ["tests/test_parity_metrics.py", "tests/test_oracle_numerics.py", "tests/test_oracle_moe.py",
+             "tests/test_oracle_router.py", "tests/test_oracle_w4a8.py"]
 
 # (file, name, text in the oracle, the mistaken text)
 MUTANTS = [
+    ('oracle/inputs.py', 'code_diffs_two_steps',
+     'adjacent = same_sign & (np.abs(gi - ri) <= 1)',
+     'adjacent = same_sign & (np.abs(gi - ri) <= 2)'),
+    ('oracle/inputs.py', 'code_diffs_sign_ignored',
+     'same_sign = (np.sign(g[diff]) == np.sign(r[diff])) | (g[diff] == 0) | (r[diff] == 0)',
+     'same_sign = np.ones(int(diff.sum()), dtype=bool)'),
+    ('oracle/inputs.py', 'out_metrics_max_over_norm',
+     'mx = np.abs(d).max() / max(np.abs(ref).max(), 1e-30)',
+     'mx = np.abs(d).max() / max(np.linalg.norm(ref), 1e-30)'),
+    ('oracle/inputs.py', 'bf16_ulps_sign_order',
+     'return np.where(bits & 0x8000, 0x8000 - bits, bits)',
+     'return np.where(bits & 0x8000, bits - 0x8000, bits)'),
     ('oracle/moe.py', 'act_scale_240',
      'scale = f32(amax / np.float32(E4M3_MAX))',
      'scale = f32(amax / np.float32(240.0))'),

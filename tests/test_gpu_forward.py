@@ -14,7 +14,8 @@ from fp8_block_scale_gb300 import _lib as L
 from fp8_block_scale_gb300 import workloads as W
 from fp8_block_scale_gb300.problem import DeviceProblem
 from oracle import moe as O
-from oracle.inputs import CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, oracle_inputs, out_metrics
+from oracle.inputs import (CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, bf16_ulps, code_diffs, oracle_inputs,
+                           out_metrics)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,14 +115,6 @@ def test_forward_small_each_path(name, mode):
     assert int(prob.status.item()) == 0
 
 
-def _bf16_ulps(a, b):
-    """Distance in BF16 steps between two float32 arrays holding BF16 values."""
-    def ordered(x):
-        bits = (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.int64)
-        return np.where(bits & 0x8000, 0x8000 - bits, bits)   # monotone in the value
-    return np.abs(ordered(a) - ordered(b))
-
-
 TIGHT = [(n, L.TILE_SINGLE) for n in SMALL] + [(n, L.TILE_VECTOR) for n in VECTOR_SMALL]
 
 
@@ -141,7 +134,7 @@ def test_forward_matches_oracle_in_its_rounding_order(name, mode):
     combine = "bf16_route" if mode == L.TILE_SINGLE else "fp32"
     ref = O.moe_forward(**inp, routed_scale=cfg.routed_scale, combine=combine)
     got = prob.out.float().cpu().numpy()
-    ulps = _bf16_ulps(got, ref)
+    ulps = bf16_ulps(got, ref)
     print(f"{name} {combine}: {int((ulps > 0).sum())} of {ulps.size} differ, max {int(ulps.max())} step")
     assert (ulps > 0).sum() <= max(2, 0.001 * ulps.size)
     assert np.abs(got.astype(np.float64) - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
@@ -211,7 +204,7 @@ def test_forward_full_size_in_its_rounding_order(name, mode, combine):
         flipped[ti] += nd
         n_codes += codes.size
     assert flipped.sum() <= max(1, CODE_DIFF_FRAC * n_codes)
-    ulps = _bf16_ulps(got, ref)
+    ulps = bf16_ulps(got, ref)
     for ti in range(tokens.size):
         print(f"{name} {combine} token {tokens[ti]}: {int(flipped[ti])} intermediate codes off, "
               f"{int((ulps[ti] > 0).sum())} of {ulps.shape[1]} outputs differ, max {int(ulps[ti].max())} step")
