@@ -1,13 +1,12 @@
 // Offline weight preparation and the quantisers that produce the path's FP8
 // inputs.
-//  - moe_prep_weights: gate/up eight-row interleave (FlashInfer PR #4287,
-//    "Public contract and review fixes": gate/up rows use the eight-row
-//    interleave).
+//  - moe_prep_weights: the eight-row gate/up interleave the forward expects
+//    (FlashInfer PR #4287, "Public contract and review fixes").
 //  - moe_requant_scales_ue8m0: FP32 -> power-of-two block scales (SGLang PR
 //    #43556, "Motivation" and "Modifications").
-//  - moe_quantize_act_1x128 / moe_quantize_weight_128x128: FP32 per-token
-//    group-128 activation scales and 128x128 weight block scales (PR #4287,
-//    "Public contract and review fixes").
+//  - moe_quantize_act_1x128 / moe_quantize_weight_128x128: one FP32 scale
+//    per token and 128 columns of activations, one per 128x128 weight block
+//    (PR #4287, "Public contract and review fixes").
 // All of them stream HBM once: coalesced 16-byte loads and stores.
 #include "common.cuh"
 

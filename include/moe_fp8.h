@@ -94,8 +94,8 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
  * Offline weight preparation.
  * ------------------------------------------------------------------------ */
 
-/* Gate/up eight-row interleave ("Gate/up rows use the provided eight-row
- * interleave", PR #4287 "Public contract and review fixes").  w13 holds
+/* Gate/up eight-row interleave (PR #4287, "Public contract and review
+ * fixes": the gate and up rows of W13 come interleaved in groups of eight).  w13 holds
  * [E, 2I, H] E4M3 codes in the logical layout (gate rows [0, I), up rows
  * [I, 2I)); w13_interleaved receives, per expert, rows 16q..16q+7 = gate rows
  * 8q..8q+7 and rows 16q+8..16q+15 = up rows I+8q..I+8q+7.  Out of place (the
@@ -121,9 +121,9 @@ moe_status moe_requant_scales_ue8m0(uint8_t* w, float* scale, uint8_t* ue8m0_exp
                                     int E, int rows, int cols, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Quantisers (the step before the path: "FP8 activations [M, K] with FP32
- * per-token group-128 scales; FP8 weights with FP32 128x128 block scales",
- * PR #4287 "Public contract and review fixes").  scale = f32(amax / 448);
+ * Quantisers (the step before the path; PR #4287, "Public contract and
+ * review fixes": activations carry one FP32 scale per token and 128 columns,
+ * weights one FP32 scale per 128x128 block).  scale = f32(amax / 448);
  * code = E4M3_rn_satfinite(f32(x / scale)) with an IEEE FP32 division; a
  * group whose amax is 0 gets scale 0 and all-zero codes.
  * ------------------------------------------------------------------------ */

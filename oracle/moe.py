@@ -5,18 +5,20 @@ for exact sums, float32 where the method's arithmetic is FP32.
 
 Page citations used below:
 
-* [FI-4287 summary]  FlashInfer PR #4287, commit summary: the fused W8A8
-  block-scale expert computation -- routed gate/up projection, SwiGLU with
-  per-token FP8 requantisation, down projection, BF16 reduce-add into a
-  caller-owned output accumulator -- over the standard
-  ``moe_align_block_size`` routing plan; blocks past the device-side
-  ``num_tokens_post_padded`` exit untouched.
+* [FI-4287 summary]  FlashInfer PR #4287, commit summary: one fused kernel
+  computes the whole W8A8 block-scaled expert layer (the gate and up
+  projections of the routed rows, SwiGLU whose output is requantised to FP8
+  per token, the down projection, and a BF16 add of each result into an
+  output buffer the caller owns and accumulates in), driven by the usual
+  ``moe_align_block_size`` plan; plan blocks at or past the padded length
+  held on the device do nothing.
 * [FI-4287 contract] same page, PR description, "Public contract and review
-  fixes": FP8 activations [M,K] with FP32 per-token group-128 scales; FP8
-  weights with FP32 128x128 block scales; gate/up rows use the eight-row
-  interleave; K % 128 == 0, N % 256 == 0, block_m >= 8 and divisible by 8;
-  sorted_token_ids.numel() >= expert_ids.numel() * block_m; the
-  zero-activation-scale branch (no 0 * infinity).
+  fixes": activations are FP8 [M,K] with one FP32 scale per token and 128
+  columns; weights are FP8 with one FP32 scale per 128x128 block; the gate
+  and up rows come interleaved in groups of eight; K is a multiple of 128,
+  N of 256, block_m at least 8 and a multiple of 8; the plan's slot array
+  has at least len(expert_ids) * block_m entries; a zero activation scale
+  takes its own branch, so 0 * infinity never arises.
 * [FI-4287 perf] same page, "Final W8 kernel performance (v46)": scales are
   applied after each dot ("down-reference post-dot scaling"); the order
   ((a*b)*r)*s vs ((a*r)*s)*b of activation, weight, route weight and routed

@@ -5,13 +5,14 @@ for exact sums, float32 where the method's arithmetic is FP32.
 
 Page citations used below:
 
-* [SM120-FP8] sglang-glm53-flash-sm120 pull request #13, description: an
-  FP8-activation path for the E2M1-K32 MoE experts -- E2M1 weight operands
-  with FP32 scales per 32 elements of K ("K32"), applied in FP32, and one
-  FP32 activation scale per row; the weights keep their prepared form; the
-  synthetic shape is 288 experts, hidden 4096, intermediate 1024, top-8; the
-  checks cover partial blocks, uneven routing, zero weight scales and masked
-  routes.
+* [SM120-FP8] sglang-glm53-flash-sm120 pull request #13, description: the
+  MoE experts whose weights are E2M1 codes with an FP32 scale for every 32
+  elements of K ("K32") get an FP8-activation path; the K32 scales are
+  applied in FP32, each activation row has one FP32 scale, and the weights
+  stay in the form they were prepared in.  Its timed shape is E = 288,
+  H = 4096, I = 1024 and top-8, and its checks include
+  blocks only partly filled with rows, routes spread unevenly over the
+  experts, experts whose weight scales are zero, and masked routes.
 * E2M1 itself is the FP4 element type of the OCP Microscaling Formats (MX)
   specification; the page only names it.
 
