@@ -204,7 +204,7 @@ def main():
             with open(target) as f:
                 original = f.read()
             if good not in original:
-                print(f"{name:28s} STALE (anchor not found in {path})")
+                print(f"{name:28s} STALE (anchor not found in {path})", flush=True)
                 stale += 1
                 continue
             with open(target, "w") as f:
@@ -219,7 +219,7 @@ def main():
             ok = r.returncode != 0
             caught += ok
             missed += not ok
-            print(f"{name:28s} {'caught' if ok else 'MISSED'}  {tail}")
+            print(f"{name:28s} {'caught' if ok else 'MISSED'}  {tail}", flush=True)
         print(f"{caught} caught, {missed} missed, {stale} stale")
         sys.exit(1 if missed or stale else 0)
     finally:
