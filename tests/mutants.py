@@ -10,6 +10,7 @@ never modified.
 
     python tests/mutants.py            # all mistakes
     python tests/mutants.py -k ue8m0   # those whose name contains "ue8m0"
+    python tests/mutants.py -j 8       # eight at a time (default: up to 4)
 
 An entry whose anchor text no longer occurs in the oracle is reported as
 stale (the oracle changed: update the entry).
@@ -17,10 +18,12 @@ stale (the oracle changed: update the entry).
 
 import argparse
 import os
+import queue
 import shutil
 import subprocess
 import sys
 import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PIN_TESTS = ["tests/test_parity_metrics.py", "tests/test_oracle_numerics.py", "tests/test_oracle_moe.py",
@@ -187,39 +190,61 @@ MUTANTS = [
 ]
 
 
+def _run_one(copy, path, good, bad, env):
+    """Plant one mistake in the given copy, run the pins there, restore."""
+    target = os.path.join(copy, path)
+    with open(target) as f:
+        original = f.read()
+    if good not in original:
+        return None, f"anchor not found in {path}"
+    with open(target, "w") as f:
+        f.write(original.replace(good, bad, 1))
+    try:
+        r = subprocess.run([sys.executable, "-m", "pytest", *PIN_TESTS, "-q", "-x", "-p", "no:cacheprovider"],
+                           cwd=copy, env=dict(env, PYTHONPATH=os.pathsep.join([copy, ROOT])),
+                           capture_output=True, text=True)
+    finally:
+        with open(target, "w") as f:
+            f.write(original)
+    return r.returncode != 0, (r.stdout.strip().splitlines() or [""])[-1]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("-k", default="", help="only mistakes whose name contains this")
+    ap.add_argument("-j", type=int, default=max(1, min(4, (os.cpu_count() or 2) // 2)),
+                    help="mistakes checked at once, each in its own copy")
     args = ap.parse_args()
+    todo = [m for m in MUTANTS if args.k in m[1]]
     tmp = tempfile.mkdtemp(prefix="oracle_mutants_")
     try:
-        for d in ("oracle", "tests"):
-            shutil.copytree(os.path.join(ROOT, d), os.path.join(tmp, d), ignore=shutil.ignore_patterns("__pycache__"))
-        env = dict(os.environ, PYTHONPATH=os.pathsep.join([tmp, ROOT]))
-        caught = missed = stale = 0
-        for path, name, good, bad in MUTANTS:
-            if args.k not in name:
-                continue
-            target = os.path.join(tmp, path)
-            with open(target) as f:
-                original = f.read()
-            if good not in original:
-                print(f"{name:28s} STALE (anchor not found in {path})", flush=True)
-                stale += 1
-                continue
-            with open(target, "w") as f:
-                f.write(original.replace(good, bad, 1))
+        copies = queue.Queue()
+        for i in range(args.j):
+            copy = os.path.join(tmp, str(i))
+            for d in ("oracle", "tests"):
+                shutil.copytree(os.path.join(ROOT, d), os.path.join(copy, d),
+                                ignore=shutil.ignore_patterns("__pycache__"))
+            copies.put(copy)
+        env = dict(os.environ)
+
+        def check(m):
+            path, name, good, bad = m
+            copy = copies.get()
             try:
-                r = subprocess.run([sys.executable, "-m", "pytest", *PIN_TESTS, "-q", "-x", "-p", "no:cacheprovider"],
-                                   cwd=tmp, env=env, capture_output=True, text=True)
+                return name, _run_one(copy, path, good, bad, env)
             finally:
-                with open(target, "w") as f:
-                    f.write(original)
-            tail = r.stdout.strip().splitlines()[-1] if r.stdout.strip() else ""
-            ok = r.returncode != 0
-            caught += ok
-            missed += not ok
-            print(f"{name:28s} {'caught' if ok else 'MISSED'}  {tail}", flush=True)
+                copies.put(copy)
+
+        caught = missed = stale = 0
+        with ThreadPoolExecutor(max_workers=args.j) as pool:
+            for name, (ok, tail) in pool.map(check, todo):
+                if ok is None:
+                    stale += 1
+                    print(f"{name:28s} STALE ({tail})", flush=True)
+                    continue
+                caught += ok
+                missed += not ok
+                print(f"{name:28s} {'caught' if ok else 'MISSED'}  {tail}", flush=True)
         print(f"{caught} caught, {missed} missed, {stale} stale")
         sys.exit(1 if missed or stale else 0)
     finally:
