@@ -31,6 +31,15 @@ PIN_TESTS = ["tests/test_parity_metrics.py", "tests/test_oracle_numerics.py", "t
 
 # (file, name, text in the oracle, the mistaken text)
 MUTANTS = [
+    ('oracle/moe.py', 'fp64_twin_routed_scale',
+     'out[t] += y * float(topk_w[t, j]) * float(routed_scale)',
+     'out[t] += y * float(topk_w[t, j])'),
+    ('oracle/moe.py', 'fp64_twin_silu_sign',
+     'h = g / (1.0 + np.exp(-g)) * u',
+     'h = g / (1.0 + np.exp(g)) * u'),
+    ('oracle/w4a8.py', 'w4_fp64_twin_route_weight',
+     'out[t] += y * float(topk_w[t, j]) * float(routed_scale)',
+     'out[t] += y * float(routed_scale)'),
     ('oracle/inputs.py', 'code_diffs_two_steps',
      'adjacent = same_sign & (np.abs(gi - ri) <= 1)',
      'adjacent = same_sign & (np.abs(gi - ri) <= 2)'),

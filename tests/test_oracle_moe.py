@@ -293,8 +293,8 @@ def _near_tie(ratio):
                                         (12, dict(M=4, H=256, I=256, E=2, k=1))])
 def test_forward_matches_fp64_brute_force(seed, shape):
     p = _tiny_problem(seed, **shape)
-    out32, inter = moe.moe_forward(**p, routed_scale=1.0, return_inter=True, round_bf16=False)
-    out64, inter64 = moe.moe_forward_fp64(**p, routed_scale=1.0)
+    out32, inter = moe.moe_forward(**p, routed_scale=2.5, return_inter=True, round_bf16=False)
+    out64, inter64 = moe.moe_forward_fp64(**p, routed_scale=2.5)
     # intermediate codes identical except where the exact value is a near-tie
     n_diff = 0
     for key, (codes, scales) in inter.items():
