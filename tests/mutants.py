@@ -31,6 +31,27 @@ PIN_TESTS = ["tests/test_parity_metrics.py", "tests/test_oracle_numerics.py", "t
 
 # (file, name, text in the oracle, the mistaken text)
 MUTANTS = [
+    ('oracle/moe.py', 'combine_bf16_route_unrounded',
+     '                y = bf16_round(y)',
+     '                y = y'),
+    ('oracle/moe.py', 'combine_bf16_stepwise_unrounded',
+     '                acc = bf16_round(acc)',
+     '                acc = acc'),
+    ('oracle/moe.py', 'act_ue8m0_not_rounded',
+     'scale = ue8m0_round_up(f32(np.max(np.abs(g), axis=-1) / np.float32(E4M3_MAX)))',
+     'scale = f32(np.max(np.abs(g), axis=-1) / np.float32(E4M3_MAX))'),
+    ('oracle/numerics.py', 'e4m3_nan_code',
+     'return np.where(nan, 0x7F, code).astype(np.uint8)',
+     'return np.where(nan, 0x7E, code).astype(np.uint8)'),
+    ('oracle/numerics.py', 'e4m3_decode_no_nan',
+     'return np.where((e == 15) & (m == 7), np.nan, val)',
+     'return val'),
+    ('oracle/numerics.py', 'bf16_no_overflow',
+     'r = np.where(r > bf16_max, np.inf, r)',
+     'r = np.minimum(r, bf16_max)'),
+    ('oracle/w4a8.py', 'e2m1_subnormal_scale',
+     'mag = np.ldexp(np.where(e == 0, m, 2 + m).astype(np.float64), np.where(e == 0, -1, e - 2))',
+     'mag = np.ldexp(np.where(e == 0, m, 2 + m).astype(np.float64), np.where(e == 0, 0, e - 2))'),
     ('oracle/moe.py', 'fp64_twin_routed_scale',
      'out[t] += y * float(topk_w[t, j]) * float(routed_scale)',
      'out[t] += y * float(topk_w[t, j])'),

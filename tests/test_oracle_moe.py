@@ -467,6 +467,13 @@ def test_forward_combine_modes():
     # per-route rounding: every contribution moves by at most 2^-8 of itself
     route = moe.moe_forward(**p, combine="bf16_route", round_bf16=False).astype(np.float64)
     assert (np.abs(route - acc) <= 2.0 ** -8 * sum(np.abs(cj) for cj in c) + slack).all()
+    assert not np.array_equal(route, acc)                 # the per-route rounding shows somewhere
+    # and it decomposes into the single-route runs: each contribution rounded
+    # to BF16 on its own, then added in slot order in FP32 onto the prior
+    s = p["out_prior"].astype(np.float32)
+    for cj in c:
+        s = f32(s + bf16_round(f32(cj)))
+    assert np.array_equal(route, s.astype(np.float64))
     # stepwise: the prior and each running sum are rounded once more
     step = moe.moe_forward(**p, combine="bf16_stepwise").astype(np.float64)
     running = [np.abs(prior)]
