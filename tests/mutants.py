@@ -31,6 +31,15 @@ PIN_TESTS = ["tests/test_parity_metrics.py", "tests/test_oracle_numerics.py", "t
 
 # (file, name, text in the oracle, the mistaken text)
 MUTANTS = [
+    ('oracle/moe.py', 'routes_slot_lost',
+     'groups[e][1].append(j)',
+     'groups[e][1].append(0)'),
+    ('oracle/moe.py', 'act_groups_transposed',
+     'codes, scale = _quantize_groups(x.reshape(M, H // GROUP, GROUP))',
+     'codes, scale = _quantize_groups(x.reshape(M, GROUP, H // GROUP).transpose(0, 2, 1))'),
+    ('oracle/numerics.py', 'e4m3_negative_zero_lost',
+     'neg = np.signbit(x)',
+     'neg = x < 0'),
     ('oracle/moe.py', 'combine_bf16_route_unrounded',
      '                y = bf16_round(y)',
      '                y = y'),
