@@ -10,7 +10,6 @@ forward's, call after call, within the forward's usual tolerances.
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
