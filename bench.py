@@ -393,9 +393,19 @@ def measure_e2e(prob, steps, warmup):
 
 # ---------------------------------------------------------------- oracle timing (CPU baseline)
 
-def _oracle_child(npz_path, groups_json):
-    """Runs in a fresh process with one BLAS/OpenMP thread: times the oracle
-    forward on each group of (local) token indices, one timing per group."""
+def oracle_workers():
+    """Host cores this process may run on: the oracle's expert-partitioned
+    threads, one BLAS thread each."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def _oracle_child(npz_path, groups_json, workers="1"):
+    """Runs in a fresh process with one BLAS/OpenMP thread per worker: times
+    the oracle forward, its experts computed in `workers` threads, on each
+    group of (local) token indices, one timing per group."""
     import numpy as np
     from oracle import moe as O
     d = dict(np.load(npz_path))
@@ -403,14 +413,15 @@ def _oracle_child(npz_path, groups_json):
     secs = []
     for g in json.loads(groups_json):
         t0 = time.perf_counter()
-        O.moe_forward(**d, routed_scale=rs, tokens=g)
+        O.moe_forward(**d, routed_scale=rs, tokens=g, workers=int(workers))
         secs.append(time.perf_counter() - t0)
     print(json.dumps({"seconds": secs}))
 
 
-def oracle_sample_seconds(cfg, routing, tokens, groups):
+def oracle_sample_seconds(cfg, routing, tokens, groups, workers=1):
     """Oracle inputs for the token sample (built here, untimed), then the oracle
-    forward timed per group of sample positions in a single-threaded child."""
+    forward timed per group of sample positions in a child process whose
+    `workers` threads each use one BLAS thread."""
     import numpy as np
     from oracle.inputs import oracle_inputs
     inp, _ = oracle_inputs(cfg, routing, tokens)
@@ -419,8 +430,8 @@ def oracle_sample_seconds(cfg, routing, tokens, groups):
     np.savez(path, routed_scale=np.float32(cfg.routed_scale), **inp)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", path, json.dumps(groups)],
-                       env=env, capture_output=True, text=True, cwd=ROOT)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", path, json.dumps(groups),
+                        str(workers)], env=env, capture_output=True, text=True, cwd=ROOT)
     os.unlink(path)
     if r.returncode != 0:
         raise RuntimeError("oracle child failed: " + r.stderr[-2000:])
@@ -440,12 +451,13 @@ def _valid_routes(cfg, routing, tokens):
 
 def cpu_baseline(cfg, routing, n_tokens=4):
     tokens = sample_tokens(cfg, n_tokens)
-    secs = sum(oracle_sample_seconds(cfg, routing, tokens, [list(range(len(tokens)))]))
+    workers = oracle_workers()
+    secs = sum(oracle_sample_seconds(cfg, routing, tokens, [list(range(len(tokens)))], workers))
     rv = _valid_routes(cfg, routing, tokens)
     flop = rv * 6 * cfg.H * cfg.I
-    return {"value": flop / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": flop / secs / 1e12, "unit": UNIT, "cores": workers, "kind": "oracle",
             "sample": f"{len(tokens)} of {cfg.M} tokens ({rv} routes) of {cfg.name}, oracle forward only, "
-                      f"one BLAS thread, {secs:.1f} s"}
+                      f"experts over {workers} threads of one BLAS thread each, {secs:.1f} s"}
 
 
 # ---------------------------------------------------------------- main
@@ -466,7 +478,8 @@ def run_reference(args, rank):
     n = args.warmup + args.steps
     pool = sample_tokens(cfg, min(n, 4))
     groups = [[i % len(pool)] for i in range(n)]
-    secs = oracle_sample_seconds(cfg, routing, pool, groups)[args.warmup:]
+    workers = oracle_workers()
+    secs = oracle_sample_seconds(cfg, routing, pool, groups, workers)[args.warmup:]
     flops = [_valid_routes(cfg, routing, pool[g]) * 6 * cfg.H * cfg.I for g in groups[args.warmup:]]
     value = sum(flops) / sum(secs) / 1e12
     ms = 1e3 * sum(secs) / len(secs)
@@ -476,8 +489,9 @@ def run_reference(args, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (numpy oracle)", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "sample": "1 token per step (all its routes)",
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"1 token of {cfg.M} per step, {args.steps} steps, one BLAS thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
+                         "sample": f"1 token of {cfg.M} per step, {args.steps} steps, experts over "
+                                   f"{workers} threads of one BLAS thread each"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -752,7 +766,7 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing (profiling runs)")
-    ap.add_argument("--oracle-child", nargs=2, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-child", nargs=3, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--w4a8", action="store_true",
                     help="time only the E2M1-K32 weight path at 1 and 1024 tokens (one JSON line)")
     args = ap.parse_args()
