@@ -470,7 +470,7 @@ def workload_desc(cfg):
 def run_reference(args, rank):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample:
     each step is one token (all of its routes) of the workload."""
-    from fp8_block_scale_gb300 import workloads as W
+    import workloads as W
     if rank != 0:
         return
     cfg = W.CONFIGS[args.workload]
@@ -536,7 +536,7 @@ def job_tflops(flop_per_rank, world, step_ms):
 def run_ours(args, rank, world, dist):
     import torch
     from fp8_block_scale_gb300 import _lib as L
-    from fp8_block_scale_gb300 import workloads as W
+    import workloads as W
     from fp8_block_scale_gb300.problem import DeviceProblem
 
     L.load()
@@ -630,7 +630,7 @@ def run_ours(args, rank, world, dist):
 def extra_sweep(cfg, prob, flush, peaks):
     """Other token counts of the same weights, and the decode workload."""
     import torch
-    from fp8_block_scale_gb300 import workloads as W
+    import workloads as W
     from fp8_block_scale_gb300.problem import DeviceProblem
     out = {}
     hbm = peaks["hbm_gbs"]
@@ -699,7 +699,7 @@ def measure_w4a8(M, flush, peaks, steps=5, warmup=3):
     experts' packed codes and K32 scales (1.875 * H * I each) + activations,
     their row scales and `out` read and written."""
     import torch
-    from fp8_block_scale_gb300 import workloads as W
+    import workloads as W
     from fp8_block_scale_gb300.problem import W4A8Problem
     cfg = W.MoEConfig(f"w4a8_e288_m{M}", M=M, H=4096, I=1024, E=288, top_k=8, block_m=16)
     p = W4A8Problem(cfg)

@@ -2,9 +2,9 @@
 
 The compute path lives in ``libmoe_fp8.so`` (CUDA kernels behind the C ABI of
 ``include/moe_fp8.h`` and, for E2M1-K32 weights, ``include/moe_w4a8.h``);
-``_lib`` is its ctypes binding, ``problem`` assembles device buffers for a
-workload using only the library's kernels, and ``workloads`` draws the
-seeded synthetic inputs.
+``_lib`` is its ctypes binding and ``problem`` assembles device buffers for a
+workload using only the library's kernels.  The seeded synthetic inputs come
+from the top-level ``workloads`` module, which the CPU oracle imports too.
 """
 
 from ._lib import (  # noqa: F401

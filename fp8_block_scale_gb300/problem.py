@@ -10,7 +10,7 @@ computes any step of the path itself.
 import torch
 
 from . import _lib as L
-from . import workloads as W
+import workloads as W
 
 
 class DeviceProblem:

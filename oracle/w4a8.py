@@ -195,7 +195,7 @@ def gemm_w4a8(xq, xs, wq, ws):
 
 def moe_forward_w4a8(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
                      out_prior, routed_scale=1.0, tokens=None, return_inter=False,
-                     round_bf16=True):
+                     round_bf16=True, workers=1):
     """Fused MoE expert forward with E2M1-K32 weights and per-row FP8
     activations, FP32 emulation ([SM120-FP8]; readings 29-34 and, for the
     steps shared with the block-FP8 path, 1, 6-8 of ``oracle.moe``).
@@ -209,7 +209,9 @@ def moe_forward_w4a8(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
     accumulator with ``round_bf16=False``); with ``return_inter`` also
     {(t, j): (codes [I], scale)} of the requantised intermediate.  A token's
     routes are added in slot order in FP32 onto the prior value, then rounded
-    once to BF16.
+    once to BF16.  ``workers`` > 1 computes the experts' routes in that many
+    threads and combines them in the same fixed order, so the output is
+    bit-identical to ``workers=1``.
     """
     M, H = a_q.shape
     E, N, _ = w13_q.shape
@@ -221,13 +223,23 @@ def moe_forward_w4a8(a_q, a_s, w13_q, w13_s, w2_q, w2_s, topk_ids, topk_w,
     rs = np.float32(routed_scale)
     route_y = {}
     inter = {}
-    for e, (ts, js) in sorted(expert_routes(topk_ids, E, tokens).items()):
+
+    def expert_part(e, ts, js):
         acc = gemm_w4a8(a_q[ts], np.asarray(a_s)[ts], w13_q[e], w13_s[e])
         h = swiglu(acc, I)
         qi, si = quantize_act_per_row(h)
         y = gemm_w4a8(qi, si, w2_q[e], w2_s[e])
         wr = f32(f32(np.asarray(topk_w)[ts, js]) * rs)
-        y = f32(y * wr[:, None])
+        return ts, js, f32(y * wr[:, None]), qi, si
+
+    groups = sorted(expert_routes(topk_ids, E, tokens).items())
+    if workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=workers) as pool:
+            parts = list(pool.map(lambda g: expert_part(g[0], *g[1]), groups))
+    else:
+        parts = [expert_part(e, ts, js) for e, (ts, js) in groups]
+    for ts, js, y, qi, si in parts:
         for n, (t, j) in enumerate(zip(ts, js)):
             route_y[(int(t), int(j))] = y[n]
             if return_inter:

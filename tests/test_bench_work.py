@@ -11,7 +11,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
-from fp8_block_scale_gb300 import workloads as W  # noqa: E402
+import workloads as W  # noqa: E402
 
 
 def test_decode_one_token_closed_form():

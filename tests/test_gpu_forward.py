@@ -11,11 +11,12 @@ import pytest
 import torch
 
 from fp8_block_scale_gb300 import _lib as L
-from fp8_block_scale_gb300 import workloads as W
+import workloads as W
 from fp8_block_scale_gb300.problem import DeviceProblem
 from oracle import moe as O
-from oracle.inputs import (CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, bf16_ulps, code_diffs, oracle_inputs,
-                           out_metrics)
+from tests.sampling import block_cover_tokens
+from oracle.inputs import (CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, bf16_ulps, code_diffs, default_workers,
+                           oracle_inputs, out_metrics)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,12 +39,13 @@ def _run(prob, debug=True, tile_mode=L.TILE_AUTO):
 def _check(prob, tokens, dq=None, ds=None, label=""):
     cfg = prob.cfg
     inp, experts = oracle_inputs(cfg, prob.routing, tokens)
+    workers = default_workers()
     # the GPU quantisers saw the same raw values: their codes must match bit for bit
     for i, e in enumerate(experts[:4]):
         assert np.array_equal(prob.w13_logical[e].cpu().numpy(), inp["w13_q"][i]), f"W13 codes of expert {e}"
         assert np.array_equal(prob.w13_scale[e].cpu().numpy().view(np.uint32), inp["w13_s"][i].view(np.uint32))
         assert np.array_equal(prob.w2[e].cpu().numpy(), inp["w2_q"][i])
-    ref, inter = O.moe_forward(**inp, routed_scale=cfg.routed_scale, return_inter=True)
+    ref, inter = O.moe_forward(**inp, routed_scale=cfg.routed_scale, return_inter=True, workers=workers)
     got = prob.out[torch.as_tensor(tokens, device="cuda")].float().cpu().numpy()
     m = out_metrics(got, ref, inp["out_prior"])
     print(f"{label} {cfg.name} tokens={len(tokens)} {m}")
@@ -142,22 +144,24 @@ def test_forward_matches_oracle_in_its_rounding_order(name, mode):
 
 # ------------------------------------------------------------------ full-size workloads, sampled tokens
 
+# None: every token; "blocks": a token set covering every plan block
 FULL = {
-    "decode_m1": None, "decode_m8": None, "decode_m64": 6,
-    "prefill_1024": 3, "prefill_2048": 2, "prefill_4096": 2, "prefill_8192": 2,
-    "skewed": 3, "large": 2,
+    "decode_m1": None, "decode_m8": None, "decode_m64": None,
+    "prefill_1024": "blocks", "prefill_2048": "blocks", "prefill_4096": "blocks", "prefill_8192": "blocks",
+    "skewed": "blocks", "large": "blocks",
 }
 
+# prefill_8192 in plan blocks of 64 rows: more than 1024 plan blocks, so the
+# GEMMs look up the expert of the blocks past the first 1024 in global memory
+# rather than in their shared-memory copy of the plan.
+MANY_BLOCKS = W.CONFIGS["prefill_8192"].with_(name="prefill_8192_bm64", block_m=64)
 
-def _full_size(name, tile_mode):
-    cfg = W.CONFIGS[name]
+
+def _full_size(name, tile_mode, cfg=None):
+    cfg = cfg or W.CONFIGS[name]
     prob = DeviceProblem(cfg)
     dq, ds = _run(prob, tile_mode=tile_mode)
-    n = FULL[name]
-    if n is None:
-        tokens = np.arange(cfg.M)
-    else:
-        tokens = np.unique(np.linspace(0, cfg.M - 1, n).astype(np.int64))
+    tokens = np.arange(cfg.M) if FULL.get(name, "blocks") is None else block_cover_tokens(prob)
     if name == "skewed":
         ids = prob.routing.topk_ids.numpy()
         z = prob.routing.zero_scale_experts[0]
@@ -166,11 +170,21 @@ def _full_size(name, tile_mode):
         tokens = np.unique(np.concatenate([tokens, masked[:1], zero[:1]]))
     _check(prob, tokens, dq, ds, "full")
     assert int(prob.status.item()) == 0
+    return prob, tokens
 
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_forward_full_size_sampled(name):
     _full_size(name, L.TILE_AUTO)
+
+
+def test_forward_more_than_1024_plan_blocks():
+    prob, tokens = _full_size(MANY_BLOCKS.name, L.TILE_AUTO, MANY_BLOCKS)
+    nblocks = int(prob.ntpp.item()) // MANY_BLOCKS.block_m
+    assert nblocks > 1024
+    # the sample holds routes of blocks past the first 1024
+    slots = np.nonzero(np.isin(prob.sorted_ids[:nblocks * 64].cpu().numpy() // MANY_BLOCKS.top_k, tokens))[0]
+    assert (slots // 64 >= 1024).sum() > 0
 
 
 @pytest.mark.parametrize("name,mode,combine", [("decode_m1", L.TILE_AUTO, "fp32"), ("decode_m8", L.TILE_VECTOR, "fp32"),
@@ -188,9 +202,10 @@ def test_forward_full_size_in_its_rounding_order(name, mode, combine):
     cfg = W.CONFIGS[name]
     prob = DeviceProblem(cfg)
     dq, ds = _run(prob, debug=True, tile_mode=mode)
-    tokens = np.unique(np.linspace(0, cfg.M - 1, min(cfg.M, 3)).astype(np.int64))
+    tokens = np.arange(cfg.M) if cfg.M <= 64 else block_cover_tokens(prob)
     inp, _ = oracle_inputs(cfg, prob.routing, tokens)
-    ref, inter = O.moe_forward(**inp, routed_scale=cfg.routed_scale, combine=combine, return_inter=True)
+    ref, inter = O.moe_forward(**inp, routed_scale=cfg.routed_scale, combine=combine, return_inter=True,
+                               workers=default_workers())
     got = prob.out[torch.as_tensor(tokens, device="cuda")].float().cpu().numpy()
     sorted_ids = prob.sorted_ids.cpu().numpy()
     P = int(prob.ntpp.item())

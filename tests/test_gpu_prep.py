@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from fp8_block_scale_gb300 import _lib as L
-from fp8_block_scale_gb300 import workloads as W
+import workloads as W
 from oracle import moe as O
 from oracle.numerics import bf16_round
 

@@ -11,10 +11,12 @@ import pytest
 import torch
 
 from fp8_block_scale_gb300 import _lib as L
-from fp8_block_scale_gb300 import workloads as W
+import workloads as W
 from fp8_block_scale_gb300.problem import W4A8Problem
 from oracle import w4a8 as OW
-from oracle.inputs import CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, oracle_inputs_w4a8, out_metrics
+from oracle.inputs import (CODE_DIFF_FRAC, MAX_ABS_TOL, REL_L2_TOL, code_diffs, default_workers, oracle_inputs_w4a8,
+                           out_metrics)
+from tests.sampling import block_cover_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -76,7 +78,8 @@ def _check(prob, tokens, dq, ds):
     for i, e in enumerate(experts[:2]):
         assert np.array_equal(OW.unpack_e2m1(prob.w13[e].cpu().numpy()), inp["w13_q"][i]), f"W13 codes of expert {e}"
         assert np.array_equal(prob.w2_scale[e].cpu().numpy().view(np.uint32), inp["w2_s"][i].view(np.uint32))
-    ref, inter = OW.moe_forward_w4a8(**inp, routed_scale=cfg.routed_scale, return_inter=True)
+    ref, inter = OW.moe_forward_w4a8(**inp, routed_scale=cfg.routed_scale, return_inter=True,
+                                     workers=default_workers())
     got = prob.out[torch.as_tensor(tokens, device="cuda")].float().cpu().numpy()
     m = out_metrics(got, ref, inp["out_prior"])
     print(f"{cfg.name} tokens={len(tokens)} {m}")
@@ -128,6 +131,16 @@ def test_w4a8_forward_page_shape_decode():
     prob = W4A8Problem(W.MoEConfig("w4a8_e288_m1", M=1, **PAGE))
     dq, ds = _run(prob)
     _check(prob, np.asarray([0]), dq, ds)
+
+
+def test_w4a8_forward_page_shape_1024_tokens():
+    """The page's timing shape at the token count the benchmark times, on a
+    token set holding a route in every plan block."""
+    prob = W4A8Problem(W.MoEConfig("w4a8_e288_m1024", M=1024, **PAGE))
+    dq, ds = _run(prob)
+    tokens = block_cover_tokens(prob)
+    assert tokens.size >= 64
+    _check(prob, tokens, dq, ds)
 
 
 def test_w4a8_all_masked_leaves_out_unchanged():

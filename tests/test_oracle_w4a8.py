@@ -297,6 +297,19 @@ def test_forward_token_permutation_and_subset():
     np.testing.assert_array_equal(w4a8.moe_forward_w4a8(**p, tokens=[3, 1]), full[[3, 1]])
 
 
+def test_forward_expert_partitioned_is_bit_identical():
+    """Experts computed in several threads, combined in the same fixed order,
+    give exactly the single-threaded output and intermediate."""
+    p = _tiny_problem(26, M=5, H=64, I=64, E=4, k=3, masked=((2, 1),))
+    a, ia = w4a8.moe_forward_w4a8(**p, return_inter=True)
+    b, ib = w4a8.moe_forward_w4a8(**p, return_inter=True, workers=3)
+    np.testing.assert_array_equal(a, b)
+    assert ia.keys() == ib.keys()
+    for key in ia:
+        np.testing.assert_array_equal(ia[key][0], ib[key][0])
+        assert ia[key][1] == ib[key][1]
+
+
 def test_forward_routed_scale_is_a_route_weight_factor():
     p = _tiny_problem(26, M=2, H=32, I=32, E=2, k=2)
     a = w4a8.moe_forward_w4a8(**p, routed_scale=2.0, round_bf16=False)

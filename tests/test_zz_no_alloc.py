@@ -5,24 +5,30 @@ it for its own pool, a plug-in that only sees this C ABI, or a latency-bound
 loop where an allocation may synchronise the device.  This entry point takes
 the same arguments as the regular forward but uses a static device array as
 scratch instead of the caller's workspace.  Its result must match the regular
-forward's, call after call, within the forward's usual tolerances.
+forward's, call after call, within the forward's usual tolerances, and the
+CPU oracle's within the forward's acceptance bar.  The cases take both
+forward paths: the tensor-core tiles (ragged, decode_m8) and the vector path
+(decode_m1, the single-token decode step such callers run most).
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import workloads as W
 from fp8_block_scale_gb300 import _lib as L
-from fp8_block_scale_gb300 import workloads as W
 from fp8_block_scale_gb300.problem import DeviceProblem
-from oracle.inputs import MAX_ABS_TOL, REL_L2_TOL, out_metrics
+from oracle import moe as O
+from oracle.inputs import MAX_ABS_TOL, REL_L2_TOL, default_workers, oracle_inputs, out_metrics
 
 pytestmark = pytest.mark.gpu
 
 CASES = {
     "ragged": W.MoEConfig("ragged", M=37, H=384, I=256, E=5, top_k=3, block_m=64, out_init="normal0.1"),
     "decode_m8": W.CONFIGS["decode_m8"],
+    "decode_m1": W.CONFIGS["decode_m1"],
 }
 
 
@@ -35,6 +41,9 @@ def test_noalloc_forward_matches_workspace_forward_twice(name):
     prob.run_forward(prob.fwd_args(out=ref))
     torch.cuda.synchronize()
     ref_np = ref.float().cpu().numpy()
+    cfg = CASES[name]
+    inp, _ = oracle_inputs(cfg, prob.routing, np.arange(cfg.M))
+    oracle_out = O.moe_forward(**inp, routed_scale=cfg.routed_scale, workers=default_workers())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         out = prob.out_prior.clone()
@@ -43,8 +52,11 @@ def test_noalloc_forward_matches_workspace_forward_twice(name):
         args.workspace_bytes = 0
         assert lib.moe_fp8_block_scale_forward_noalloc(ctypes.byref(args), stream) == 0
         torch.cuda.synchronize()
-        m = out_metrics(out.float().cpu().numpy(), ref_np)
+        got = out.float().cpu().numpy()
+        m = out_metrics(got, ref_np)
         assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, (call, m)
+        m = out_metrics(got, oracle_out)
+        assert m["rel_l2"] <= REL_L2_TOL and m["max_rel"] <= MAX_ABS_TOL, (call, "oracle", m)
         assert int(prob.status.item()) == 0
 
 

@@ -1,8 +1,9 @@
 """Seeded synthetic workloads for the block-scaled FP8 MoE path.
 
 This module only draws random numbers and builds routings; it holds none of
-the method's arithmetic (no quantisation, no plan, no GEMM).  Both the CPU
-oracle and the GPU library consume what it produces: raw BF16 activations and
+the method's arithmetic (no quantisation, no plan, no GEMM).  It sits beside,
+not inside, the library package and the oracle: each of them imports it and
+neither imports the other.  Both consume what it produces: raw BF16 activations and
 weights are quantised afterwards, by the oracle's quantiser on the CPU side
 and by the library's quantiser kernels on the GPU side.
 
