@@ -123,6 +123,8 @@ _SIGS = {
                                                      ctypes.c_int, ctypes.c_int, ctypes.c_int64]),
     "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_fp8_block_scale_forward": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_void_p]),
     "moe_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "moe_fp8_block_scale_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(MoeFwdArgs), ctypes.c_void_p]),
     "moe_quantize_act_per_row": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
@@ -286,6 +288,13 @@ def set_profile_events(args, events):
 
 def moe_fp8_block_scale_forward(args, stream=None):
     _check("moe_fp8_block_scale_forward", load().moe_fp8_block_scale_forward(ctypes.byref(args), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(limit_us, device_status, elapsed_ns, stream=None):
+    """Run the bounded-wait self-test; returns the raw status (MOE_ERR_TIMEOUT,
+    8, is the expected outcome).  device_status: int32 [1], elapsed_ns:
+    int64 [2] device tensors."""
+    return load().moe_selftest_wait_timeout(int(limit_us), _ptr(device_status), _ptr(elapsed_ns), _stream(stream))
 
 
 def moe_noalloc_scratch_bytes():

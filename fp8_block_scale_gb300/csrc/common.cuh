@@ -74,6 +74,12 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
 // A bounded wait gives up after this long (the whole forward takes well under
 // a millisecond; one second means something is stuck).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// ... or after this many polls, whichever comes first: a second bound that
+// does not rely on %globaltimer advancing.  A failed poll takes at least some
+// ten nanoseconds (at most a short, hardware-defined suspension), so the cap
+// is a few tenths of a second or more; either bound lies far above any wait
+// of a healthy forward (milliseconds at most).
+constexpr uint32_t kWaitMaxPolls = 1u << 25;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -120,9 +126,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false, and
-// raises *abort_flag, if the wait runs past kWaitLimitNs; returns false at
-// once if another thread of the CTA has already raised *abort_flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// raises *abort_flag, if the wait runs past `limit_ns` (or kWaitMaxPolls
+// polls); returns false at once if another thread of the CTA has already
+// raised *abort_flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   unsigned long long t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -131,7 +139,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       unsigned long long now = global_timer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns || i >= kWaitMaxPolls) {
         *abort_flag = 1;
         return false;
       }

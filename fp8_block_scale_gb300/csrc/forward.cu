@@ -143,9 +143,10 @@ struct GemmParams {
   uint32_t* gen;               // up: forward stamp, advanced once per forward
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, limit_ns) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -609,9 +610,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool have = true;  // this CTA holds the tile's complete sum
       if (kUp && !kPair && p.splits > 1) {
         // split K: add this split's partial into the tile's zeroed sum; the
-        // split that arrives last reads the total back and finishes the tile
+        // split that arrives last reads the total back and finishes the tile.
+        // Every split takes its ticket, even one whose waits ran out (it adds
+        // nothing then), and the last one clears all the tile's rows, so the
+        // tickets and sums are back to zero after any forward.
         const bool live = ok && MOE_RVALID && ctl->row_tok[row] >= 0;
-        float* srow = p.usum + ((static_cast<int64_t>(b) * p.ntiles_n + t) * p.block_m + (live ? row : 0)) * kTileN +
+        float* srow = p.usum + ((static_cast<int64_t>(b) * p.ntiles_n + t) * p.block_m + (MOE_RVALID ? row : 0)) *
+                                   kTileN +
                       128 * half;
         if (live) {
 #pragma unroll
@@ -621,7 +626,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         named_barrier(1, 32 * kNumEpiWarps);
         if (warp == 2 && lane == 0) {
           int32_t* cnt = p.ucnt + static_cast<int64_t>(b) * p.ntiles_n + t;
-          const int old = ok ? atomicAdd(cnt, 1) : -1;
+          const int old = atomicAdd(cnt, 1);
           const bool last = old == p.splits - 1;
           if (last) *cnt = 0;
           ctl->last_flag = last ? 1 : 0;
@@ -630,7 +635,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         have = ctl->last_flag != 0;
         if (have) {
           __threadfence();
-          if (live) {
+          if (MOE_RVALID) {
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
               const float4 v = __ldcg(reinterpret_cast<const float4*>(srow + c));
@@ -916,6 +921,33 @@ __global__ void __launch_bounds__(256) combine_kernel(uint16_t* __restrict__ out
 }
 
 
+// Self-test of the failure detection.  Warp 0 waits, through the pipelines'
+// bounded wait, on an mbarrier that nothing arrives at, giving up after
+// `limit_ns`; warp 1 waits on a second such barrier with the pipelines'
+// normal limit and must stop as soon as warp 0 raises the CTA's abort flag.
+// The CTA then reports MOE_DEV_TIMEOUT as a GEMM CTA whose wait ran out does.
+// elapsed_ns[w] receives how long warp w waited.
+__global__ void __launch_bounds__(64, 1)
+    wait_selftest_kernel(int32_t* status, unsigned long long limit_ns, unsigned long long* elapsed_ns) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const unsigned long long t0 = global_timer_ns();
+  const bool ok = warp == 0 ? warp_wait(smem_u32(&bars[0]), 0, &abort_flag, limit_ns)
+                            : warp_wait(smem_u32(&bars[1]), 0, &abort_flag);
+  const unsigned long long t1 = global_timer_ns();
+  if ((threadIdx.x & 31) == 0) elapsed_ns[warp] = ok ? 0ull : t1 - t0;
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) report(status, MOE_DEV_TIMEOUT);
+}
+
 // Activation rows are copied into plan order when plan blocks are well
 // filled (at least 8 routes per touched expert on average): tile::gather4
 // moves one 128-byte row per ~35 cycles per SM on GB300, far below the rate
@@ -1042,6 +1074,23 @@ extern "C" {
 size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int block_m, int64_t sorted_cap) {
   if (M < 0 || H < 0 || I < 0 || E < 1 || top_k < 1 || block_m < 1 || sorted_cap < 0) return 0;
   return moe::ws_layout(M, H, I, E, top_k, block_m, sorted_cap).total;
+}
+
+moe_status moe_selftest_wait_timeout(uint32_t limit_us, int32_t* device_status, uint64_t* elapsed_ns,
+                                     moe_stream_t stream) {
+  using namespace moe;
+  if (!device_status || !elapsed_ns) return MOE_ERR_NULL;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_SHAPE;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if (!on_device(device_status, dev.device) || !on_device(elapsed_ns, dev.device)) return MOE_ERR_DEVICE;
+  wait_selftest_kernel<<<1, 64, 0, stream>>>(device_status, 1000ull * limit_us,
+                                             reinterpret_cast<unsigned long long*>(elapsed_ns));
+  MOE_CUDA_TRY(cudaGetLastError());
+  MOE_CUDA_TRY(cudaStreamSynchronize(stream));
+  int32_t st = 0;
+  MOE_CUDA_TRY(cudaMemcpy(&st, device_status, sizeof(st), cudaMemcpyDeviceToHost));
+  return (st & MOE_DEV_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_OK;
 }
 
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t stream) {

@@ -12,7 +12,10 @@
  * Conventions shared by every entry point:
  *  - Pointers are DEVICE pointers on the current CUDA device unless the
  *    argument says otherwise; the caller owns every buffer.  The library
- *    allocates no device memory and keeps no per-call global state.
+ *    allocates no device memory and keeps no per-call global state, with
+ *    one exception: the allocation-free forward at the end of this header
+ *    draws its scratch from a fixed static device array (32 MiB per GPU
+ *    that loads the library) that all of its calls share.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Argument errors are detected on the host and returned
  *    before anything is launched; a failed launch returns MOE_ERR_CUDA.
@@ -43,11 +46,18 @@ typedef enum {
   MOE_ERR_DTYPE = 5,    /* unsupported id width                               */
   MOE_ERR_DEVICE = 6,   /* pointer not on the current device / not sm_103     */
   MOE_ERR_CUDA = 7,     /* a CUDA runtime/driver call failed                  */
-  MOE_ERR_TIMEOUT = 8   /* reserved for host-visible timeouts                 */
+  MOE_ERR_TIMEOUT = 8   /* a synchronous call saw a device wait run out (only
+                           moe_selftest_wait_timeout blocks on the device and
+                           returns it; asynchronous calls report device
+                           timeouts as MOE_DEV_TIMEOUT in *device_status)    */
 } moe_status;
 
 /* Bits OR-ed into *device_status by the kernels. */
-#define MOE_DEV_TIMEOUT 0x1         /* a bounded pipeline wait ran out; the CTA stopped */
+#define MOE_DEV_TIMEOUT 0x1         /* a bounded pipeline wait ran out (after 1 s, or
+                                       2^25 polls); the CTA stopped.  The
+                                       results of that call are invalid and its
+                                       workspace may hold stale sums: zero it
+                                       again (moe_workspace_init) before reuse */
 #define MOE_DEV_BAD_EXPERT 0x2      /* a plan block named an expert outside [0, E) other than -1 */
 
 /* Human-readable name of a status code (static string). */
@@ -270,7 +280,8 @@ size_t moe_forward_workspace_size(int64_t M, int H, int I, int E, int top_k, int
  * split-K tickets and partial sums go back to zero, and each route's flag
  * holds the stamp of the last forward whose plan held it, against a stamp
  * counter the gate/up kernel advances once per forward (so a replayed CUDA
- * graph stays correct).  The layout depends on the sizes, so before a
+ * graph stays correct).  A forward that set MOE_DEV_TIMEOUT may leave it
+ * dirty: zero it again before the next forward.  The layout depends on the sizes, so before a
  * forward with other sizes zero the workspace again (or use another one).
  * The BF16 route contributions, the first M * top_k * H * 2 bytes, are
  * scratch written before they are read.  Two forwards that share a
@@ -283,6 +294,26 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_strea
  * pointers on the current device, which must be sm_103 (GB300: the library
  * is built for sm_103a only). */
 moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t stream);
+
+/* Failure-detection self-test (the pages have no counterpart: it exercises
+ * this library's bounded waits, the GB300 replacement for a hang).  Launches
+ * one CTA on `stream` whose first warp waits, through the GEMM pipelines'
+ * own bounded mbarrier wait, on a barrier that nothing arrives at and gives
+ * up after limit_us microseconds; its second warp waits on another such
+ * barrier with the pipelines' normal one-second limit and must stop as soon
+ * as the first raises the CTA's abort flag.  The CTA then ORs
+ * MOE_DEV_TIMEOUT into *device_status as a GEMM CTA whose wait ran out does,
+ * and writes how long each warp waited, in nanoseconds, to elapsed_ns[0]
+ * and elapsed_ns[1] (0 for a wait that completed).  Nothing traps or
+ * faults: the context stays usable.
+ *  device_status  [1] int32, device memory, caller-owned (OR-ed into)
+ *  elapsed_ns     [2] uint64, device memory, caller-owned (written)
+ * Blocks until the kernel has finished (not capturable in a CUDA graph),
+ * then returns MOE_ERR_TIMEOUT if *device_status holds MOE_DEV_TIMEOUT (the
+ * expected outcome), MOE_OK otherwise.  1 <= limit_us <= 1000000, else
+ * MOE_ERR_SHAPE. */
+moe_status moe_selftest_wait_timeout(uint32_t limit_us, int32_t* device_status, uint64_t* elapsed_ns,
+                                     moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free forward.  The pages have no counterpart to this entry
@@ -307,6 +338,9 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* args, moe_stream_t st
  * host-side set-up step); make that first call before any stream capture.
  * Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
  * ------------------------------------------------------------------------ */
+/* The address looked up on a device's first call is kept for the life of the
+ * process: do not use this entry point on a device after cudaDeviceReset (or
+ * anything else that destroys and recreates its primary context). */
 size_t moe_noalloc_scratch_bytes(void);
 moe_status moe_fp8_block_scale_forward_noalloc(const moe_fwd_args* args, moe_stream_t stream);
 

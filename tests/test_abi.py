@@ -218,3 +218,12 @@ def test_w4a8_workspace_size(lib):
         assert lib.moe_w4a8_workspace_size(M, H, I, k) == want
     assert lib.moe_w4a8_workspace_size(-1, 256, 128, 2) == 0
     assert lib.moe_w4a8_workspace_size(4, 256, 128, 0) == 0
+
+
+def test_selftest_host_validation_without_gpu(lib):
+    """The failure-detection self-test checks its arguments on the host."""
+    f = lib.moe_selftest_wait_timeout
+    assert f(1000, None, _fake(256), None) == 1                  # MOE_ERR_NULL
+    assert f(1000, _fake(256), None, None) == 1
+    assert f(0, _fake(256), _fake(512), None) == 2               # limit below 1 us
+    assert f(1000001, _fake(256), _fake(512), None) == 2         # limit above 1 s
