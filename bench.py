@@ -443,6 +443,15 @@ def sample_tokens(cfg, n, offset=0):
     return np.unique((np.linspace(0, cfg.M - 1, n).astype(np.int64) + offset) % cfg.M)
 
 
+def _expert_groups(cfg, routing, tokens):
+    """Distinct experts the tokens' valid routes touch: the oracle computes
+    each expert's routes in one thread, so at most this many threads work."""
+    import numpy as np
+    import torch
+    ids = routing.topk_ids.to(torch.int64).numpy()[np.asarray(tokens)]
+    return int(np.unique(ids[(ids >= 0) & (ids < cfg.E)]).size)
+
+
 def _valid_routes(cfg, routing, tokens):
     import torch
     ids = routing.topk_ids.to(torch.int64).numpy()[tokens]
@@ -451,7 +460,8 @@ def _valid_routes(cfg, routing, tokens):
 
 def cpu_baseline(cfg, routing, n_tokens=4):
     tokens = sample_tokens(cfg, n_tokens)
-    workers = oracle_workers()
+    # threads beyond the sample's expert count would have nothing to do
+    workers = max(1, min(oracle_workers(), _expert_groups(cfg, routing, tokens)))
     secs = sum(oracle_sample_seconds(cfg, routing, tokens, [list(range(len(tokens)))], workers))
     rv = _valid_routes(cfg, routing, tokens)
     flop = rv * 6 * cfg.H * cfg.I
@@ -478,7 +488,8 @@ def run_reference(args, rank):
     n = args.warmup + args.steps
     pool = sample_tokens(cfg, min(n, 4))
     groups = [[i % len(pool)] for i in range(n)]
-    workers = oracle_workers()
+    # one token per step: at most its top_k experts keep threads busy
+    workers = max(1, min(oracle_workers(), min(_expert_groups(cfg, routing, pool[g]) for g in groups)))
     secs = oracle_sample_seconds(cfg, routing, pool, groups, workers)[args.warmup:]
     flops = [_valid_routes(cfg, routing, pool[g]) * 6 * cfg.H * cfg.I for g in groups[args.warmup:]]
     value = sum(flops) / sum(secs) / 1e12
