@@ -21,6 +21,7 @@ STATUS_NAMES = {
 }
 MOE_DEV_TIMEOUT = 0x1
 MOE_DEV_BAD_EXPERT = 0x2
+MOE_DEV_BAD_SCALE = 0x4
 
 
 class MoeError(RuntimeError):
@@ -59,10 +60,12 @@ class MoeFwdArgs(ctypes.Structure):
         ("routed_scale", ctypes.c_float),
         ("profile_events", ctypes.POINTER(ctypes.c_void_p)),
         ("tile_mode", ctypes.c_int32),
+        ("scale_mode", ctypes.c_int32),
     ]
 
 
 TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_VECTOR = 0, 1, 2, 3
+SCALES_FP32, SCALES_UE8M0 = 0, 1
 
 
 class MoeW4A8Args(ctypes.Structure):

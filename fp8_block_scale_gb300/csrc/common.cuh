@@ -214,6 +214,48 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, kind::mxf8f6f4 with one UE8M0
+// scale per row of A and per column of B for the instruction's 32-wide K
+// block (scale_vec::1X), read from tensor memory: row m of A at lane m,
+// column sfa + m / 32; column n of B at lane 32 (m / 32) + n % 32 (each lane
+// quarter holds a copy), column sfb + n / 32; the byte of each 32-bit cell
+// is chosen by the instruction descriptor's scale-factor ids.
+__device__ __forceinline__ void umma_mx8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> tensor memory copy of 32 rows x 16 bytes, written to the
+// same 32 lanes of all four lane quarters (columns taddr .. taddr + 3: row r
+// lands in lane 32 q + r, bytes 4 i .. 4 i + 3 of the row in column
+// taddr + i).  Ordered with the MMAs the same thread issues.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory descriptor of 32 rows x 16 bytes stored row after row
+// (no swizzle: 8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address
+  d |= static_cast<uint64_t>(128 >> 4) << 16;          // leading byte offset (one 16-byte column: unused)
+  d |= static_cast<uint64_t>(128 >> 4) << 32;          // stride byte offset: next 8-row core matrix
+  d |= static_cast<uint64_t>(1) << 46;                 // descriptor version (sm_100 family)
+  return d;                                            // swizzle: none
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// tensor core's (async proxy) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, rows of 128 bytes stored
 // with the 128-byte swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
@@ -232,6 +274,17 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
          | (0u << 7) | (0u << 10)                  // A, B format E4M3
          | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with UE8M0 block scales: E4M3 x
+// E4M3 -> F32, both K-major, scale-factor byte 0 of A's and B's cells.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n) {
+  return (0u << 4)                                 // B scale-factor id
+         | (0u << 7) | (0u << 10)                  // A, B format E4M3
+         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
+         | (1u << 23)                              // scale format UE8M0
+         | (static_cast<uint32_t>(m >> 4) << 24)   // M / 16
+         | (0u << 29);                             // A scale-factor id
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane

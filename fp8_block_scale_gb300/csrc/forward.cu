@@ -89,7 +89,12 @@ struct SmemCtl {
   int last_flag;                   // split-K: this CTA completed the tile's sum
   int pad;
   union alignas(16) Scratch {
-    float xchg[2][2][kTileM];                   // up: [tile parity][column half][row] amax exchange
+    struct {
+      float xchg[2][2][kTileM];                 // [tile parity][column half][row] amax exchange
+      // block-scaled mode: per stage, the slice's UE8M0 scale-factor rows
+      // for the tensor-memory copy (A: 32 rows x 16 bytes, then B)
+      alignas(16) uint8_t sf[kMaxStages][1024];
+    } up;
     uint32_t yt[kNumEpiWarps][32][20];          // down: per-warp transpose of 32 rows x 32 BF16 (padded rows)
   } u;
   int32_t row_tok[kTileM];         // up with split K: token of each tile row (-1 = no route)
@@ -106,6 +111,24 @@ constexpr size_t smem_bytes() {
          sizeof(SmemCtl);
 }
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
+
+// Tensor-memory columns of the block-scaled mode: the accumulator (one
+// 256-column buffer: a tile accumulates over all its K slices), then per
+// stage 16 columns of scale factors (A at +0..3, B at +4..11).
+constexpr uint32_t kSfTmemCol = kTileN;
+constexpr uint32_t kIdescMx = idesc_mx_e4m3(kTileM, kTileN);
+
+// A UE8M0 scale must be +0 or a normal power of two (exponent field 1..254,
+// zero mantissa, positive).
+__device__ __forceinline__ bool ue8m0_ok(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  return bits == 0u || ((bits & 0x807FFFFFu) == 0u && (bits >> 23) != 0xFFu);
+}
+// The exponent byte of a power-of-two FP32 scale (0 for +0, i.e. 2^-127),
+// in all four bytes of a tensor-memory cell.
+__device__ __forceinline__ uint32_t ue8m0_word(float v) {
+  return ((__float_as_uint(v) >> 23) & 0xFFu) * 0x01010101u;
+}
 
 struct GemmParams {
   const int32_t* expert_ids;
@@ -266,10 +289,15 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
       : "memory");
 }
 
-template <bool kUp, bool kPair>
+// kBS (gate/up, single CTAs only): both operands' scales are powers of two,
+// applied by the tensor core (kind::mxf8f6f4.block_scale) as UE8M0 scale
+// factors; a tile accumulates over all its K slices in tensor memory and the
+// epilogue reads it once, with no per-slice promotion.
+template <bool kUp, bool kPair, bool kBS = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
+  static_assert(!kBS || (kUp && !kPair), "block-scaled mode: gate/up on single CTAs");
   using C = Cfg<kPair>;
   constexpr int kStages = C::kStages;
   constexpr int kBStage = C::kBStage;
@@ -292,7 +320,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->xfull[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1 + kNumEpiWarps);  // MMA commit + every local epilogue warp
+      // MMA commit + every local epilogue warp (block-scaled: the MMA warp
+      // alone reads the stage's side data)
+      mbar_init(smem_u32(&ctl->empty[s]), kBS ? 1 : 1 + kNumEpiWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -468,6 +498,81 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         drain_wait(smem_u32(&ctl->xfull[j % kStages]), (j / kStages) & 1u);
       }
     }
+  } else if (warp == 1 && kBS) {
+    // ------------------------------------------------------------ block-scaled MMA issuer
+    // The whole warp turns each slice's FP32 power-of-two scales into UE8M0
+    // scale-factor rows in shared memory (lane r: A rows r, 32+r, 64+r, 96+r;
+    // B columns 32 i + r, which in the interleaved tile are gate columns for
+    // r % 16 < 8 and up columns otherwise); lane 0 copies them into the
+    // stage's tensor-memory columns and issues the slice's four MMAs, which
+    // accumulate into the tile's one buffer.
+    uint8_t* sf_smem = &ctl->u.up.sf[0][0];
+    uint32_t it = 0, tcount = 0;
+    bool ok = true, bad = false;
+    for (int64_t tile = MOE_CTA_ID; tile < total && ok; tile += MOE_CTA_COUNT) {
+      int b, t, sp, e;
+      if (!tile_coords<kPair>(p, ctl, tile, nvalid, b, t, sp, e)) continue;
+      const int kb0 = sp * p.ksplit;
+      const int kb1 = min(p.nkb, kb0 + p.ksplit);
+      // the accumulator is free once the epilogue has read the previous tile
+      if (!warp_wait(smem_u32(&ctl->tempty[0]), (tcount & 1u) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        // side data first: the stage (and its scale-factor slot) is free again once it has landed
+        if (!warp_wait(smem_u32(&ctl->xfull[s]), ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const StageExtra* x = sX + s;
+        uint8_t* sfa = sf_smem + s * 1024;
+        uint8_t* sfb = sfa + 512;
+        // (the staging kernel checks the activation scales of the rows that
+        // hold a route; pad rows' products are never stored)
+        uint32_t wa[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wa[i] = ue8m0_word(x->a_scale[32 * i + lane]);
+        const float4 ws = x->w_scale;
+        bad |= !ue8m0_ok(ws.x) || !ue8m0_ok(ws.y);
+        const uint32_t wb = ue8m0_word((lane & 8) ? ws.y : ws.x);
+        *reinterpret_cast<uint4*>(sfa + 16 * lane) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(sfb + 16 * lane) = make_uint4(wb, wb, wb, wb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        int okl = 1;
+        if (lane == 0) okl = mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, okl, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t tsf = tmem_base + kSfTmemCol + 16u * s;
+          tmem_cp_32x128b_warpx4(tsf, rows16_desc(smem_u32(sfa)));       // A rows 0..127
+          tmem_cp_32x128b_warpx4(tsf + 4, rows16_desc(smem_u32(sfb)));   // B columns 0..127
+          tmem_cp_32x128b_warpx4(tsf + 8, rows16_desc(smem_u32(sfb)));   // B columns 128..255 (same pattern)
+          const uint32_t a0 = smem_u32(sA + s * kABytes);
+          const uint32_t b0 = smem_u32(sB + s * kBStage);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 32; ++kk)
+            umma_mx8(tmem_base, sw128_kmajor_desc(a0 + 32u * kk), sw128_kmajor_desc(b0 + 32u * kk), kIdescMx, tsf,
+                     tsf + 4, (kb > kb0 || kk > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&ctl->empty[s]));
+          if (kb == kb1 - 1) umma_commit(smem_u32(&ctl->tfull[0]));
+        }
+        __syncwarp();
+        ++it;
+      }
+      ++tcount;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, MOE_DEV_BAD_SCALE);
+    // no MMA or copy may still be writing tensor memory when it is released:
+    // the last slice's commit on its stage's empty barrier covers them all
+    if (lane == 0 && it > 0) drain_wait(smem_u32(&ctl->empty[(it - 1) % kStages]), ((it - 1) / kStages) & 1u);
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader of a pair)
     if (lane == 0 && rank == 0) {
@@ -543,7 +648,29 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
       const int kb0 = sp * p.ksplit;
       const int kb1 = min(p.nkb, kb0 + p.ksplit);
-      for (int kb = kb0; kb < kb1; ++kb) {
+      if (kBS) {
+        // the tile's sum, scaled by the tensor core, in the one accumulator
+        if (ok) ok = warp_wait(smem_u32(&ctl->tfull[0]), tcount & 1u, abort_flag);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(lane_base + 128u * half + 16u * ch, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[16 * ch + i] = __uint_as_float(v[i]);
+          }
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
+        if (p.splits > 1) {
+          const int64_t slot = static_cast<int64_t>(b) * p.block_m + row;
+          ctl->row_tok[row] = row < p.block_m ? p.slot_route[slot] : -1;
+        }
+      }
+      for (int kb = kb0; kb < (kBS ? kb0 : kb1); ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         const uint32_t tb = it & 1u;
@@ -661,9 +788,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             amax = fmaxf(amax, fabsf(h));
           }
         }
-        ctl->u.xchg[tcount & 1][half][row] = amax;
+        ctl->u.up.xchg[tcount & 1][half][row] = amax;
         named_barrier(1, 32 * kNumEpiWarps);
-        amax = fmaxf(amax, ctl->u.xchg[tcount & 1][half ^ 1][row]);
+        amax = fmaxf(amax, ctl->u.up.xchg[tcount & 1][half ^ 1][row]);
         const float s = __fdiv_rn(amax, 448.0f);
         // h / s as h * (1/s): the two roundings can move a value across an
         // E4M3 rounding midpoint only when it lies within an ulp of it
@@ -764,6 +891,8 @@ struct StageParams {
   uint32_t* rvalid;           // [R] set to this forward's stamp for each route the plan holds
   const uint32_t* gen;        // stamp of the previous forward (this one's is gen + 1)
   float* slot_w;              // [cap_pad]
+  int32_t* status;            // nullable
+  int check_pow2;             // block-scaled mode: activation scales must be +0 or normal powers of two
   float4* wsu;                // [nblocks, I/128, H/128]
   float4* wsd;                // [nblocks, ceil(H/256), I/128]
   int64_t nblocks;
@@ -798,7 +927,11 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
       if (route) p.rvalid[id] = *p.gen + 1u;
     }
     if (!route) continue;
-    for (int k = lane; k < nkb; k += 32) p.as_t[k * p.cap_pad + slot] = __ldg(p.a_scale + tok * nkb + k);
+    for (int k = lane; k < nkb; k += 32) {
+      const float v = __ldg(p.a_scale + tok * nkb + k);
+      p.as_t[k * p.cap_pad + slot] = v;
+      if (p.check_pow2 && !ue8m0_ok(v)) report(p.status, MOE_DEV_BAD_SCALE);
+    }
     if (p.a_sorted) {
       // up to 4 KB of the row in flight per warp (8 loads per lane) before the stores
       const uint4* src = reinterpret_cast<const uint4*>(p.a + tok * p.H);
@@ -1060,7 +1193,9 @@ bool set_smem_attrs(int device) {
       cudaFuncSetAttribute(moe_gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes<true>())) != cudaSuccess ||
       cudaFuncSetAttribute(moe_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_bytes<true>())) != cudaSuccess)
+                           static_cast<int>(smem_bytes<true>())) != cudaSuccess ||
+      cudaFuncSetAttribute(moe_gemm_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<false>())) != cudaSuccess)
     return false;
   done[device] = true;
   return true;
@@ -1103,6 +1238,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   if (a->tile_mode != MOE_TILE_AUTO && a->tile_mode != MOE_TILE_SINGLE && a->tile_mode != MOE_TILE_PAIR &&
       a->tile_mode != MOE_TILE_VECTOR)
     return MOE_ERR_SHAPE;
+  if (a->scale_mode != MOE_SCALES_FP32 && a->scale_mode != MOE_SCALES_UE8M0) return MOE_ERR_SHAPE;
   if (a->blocks_cap < 1 || a->sorted_cap < a->blocks_cap * a->block_m) return MOE_ERR_CAPACITY;
   const int64_t R = a->M * a->top_k;
   if (R >= (int64_t(1) << 31) - 1 || static_cast<int64_t>(a->E) * 2 * a->I >= (int64_t(1) << 31) ||
@@ -1204,7 +1340,10 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
   // every weight tile, but per K slice the pair runs no faster than a single
   // CTA: the slice's FP32 promotion in the epilogue, not the operand stream,
   // paces the two TMEM buffers.  So the automatic choice stays single.
-  const bool want_pair = a->tile_mode == MOE_TILE_PAIR;
+  // Power-of-two scales on both operands: the gate/up GEMM applies them in
+  // the tensor core (single CTAs; a pair request runs single CTAs then).
+  const bool block_scaled = a->scale_mode == MOE_SCALES_UE8M0;
+  const bool want_pair = a->tile_mode == MOE_TILE_PAIR && !block_scaled;
   const int pair_clusters =
       want_pair && wl.pregather && nblocks <= kMaxBlocksSmem ? max_pair_clusters(dev.device, dev.sms) : 0;
   const bool pair = pair_clusters > 0;
@@ -1251,6 +1390,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     sp.H = a->H;
     sp.I = a->I;
     sp.routed_scale = a->routed_scale;
+    sp.status = a->device_status;
+    sp.check_pow2 = block_scaled ? 1 : 0;
     int64_t sgrid = ceil_div(nblocks * a->block_m, 8);
     if (sgrid > static_cast<int64_t>(dev.sms) * 8) sgrid = static_cast<int64_t>(dev.sms) * 8;
     MOE_CUDA_TRY(launch_pdl(stage_kernel, dim3(static_cast<unsigned>(sgrid)), dim3(256), 0, stream, 1, sp));
@@ -1306,6 +1447,10 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       if (clusters > pair_clusters) clusters = pair_clusters;
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, true>, dim3(static_cast<unsigned>(2 * clusters)),
                               dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_a, tm_w13, up));
+    } else if (block_scaled) {
+      const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
+      MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false, true>, dim3(up_grid), dim3(kNumThreads),
+                              smem_bytes<false>(), stream, 1, tm_a, tm_w13, up));
     } else {
       const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false>, dim3(up_grid), dim3(kNumThreads), smem_bytes<false>(),

@@ -101,12 +101,13 @@ class DeviceProblem:
         L.moe_plan(self.topk_ids, self.cfg.E, self.cfg.block_m, self.sorted_ids, self.expert_ids, self.ntpp,
                    self.plan_ws, stream)
 
-    def fwd_args(self, debug_q=None, debug_s=None, out=None, tile_mode=L.TILE_AUTO):
+    def fwd_args(self, debug_q=None, debug_s=None, out=None, tile_mode=L.TILE_AUTO, scale_mode=L.SCALES_FP32):
         args = L.make_fwd_args(self.a, self.a_scale, self.w13, self.w13_scale, self.w2, self.w2_scale,
                                self.topk_weights, self.sorted_ids, self.expert_ids, self.ntpp,
                                self.out if out is None else out, self.workspace, self.cfg.top_k, self.cfg.block_m,
                                self.cfg.routed_scale, self.status, debug_q, debug_s)
         args.tile_mode = tile_mode
+        args.scale_mode = scale_mode
         return args
 
     def run_forward(self, args=None, stream=None):

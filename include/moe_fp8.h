@@ -59,6 +59,9 @@ typedef enum {
                                        workspace may hold stale sums: zero it
                                        again (moe_workspace_init) before reuse */
 #define MOE_DEV_BAD_EXPERT 0x2      /* a plan block named an expert outside [0, E) other than -1 */
+#define MOE_DEV_BAD_SCALE 0x4       /* MOE_SCALES_UE8M0: an activation or weight block scale
+                                       the gate/up GEMM read is not +0 or a normal power of
+                                       two (the call's results are invalid)                */
 
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
@@ -236,6 +239,7 @@ typedef struct moe_fwd_args {
                                               are empty: its two kernels are timed as the
                                               gate/up and down intervals                     */
   int32_t tile_mode;                       /* MOE_TILE_*: how the GEMM tiles map to CTAs    */
+  int32_t scale_mode;                      /* MOE_SCALES_*: how the block scales are applied */
 } moe_fwd_args;
 
 /* tile_mode values.  Every mode computes the same result (up to FP32
@@ -263,6 +267,33 @@ typedef struct moe_fwd_args {
 #define MOE_TILE_SINGLE 1
 #define MOE_TILE_PAIR 2
 #define MOE_TILE_VECTOR 3
+
+/* scale_mode values (SGLang PR #43556, "Motivation" and "Modifications":
+ * block scales requantised to powers of two, the UE8M0 form that grouped
+ * FP8 GEMMs with hardware block scaling consume).
+ *   MOE_SCALES_FP32  (0, default) any FP32 block scales: every 128-wide K
+ *                    slice's partial sum is promoted in FP32 by the
+ *                    epilogue (acc += dot * a_scale * w_scale).
+ *   MOE_SCALES_UE8M0 the caller guarantees that every activation scale
+ *                    (a_scale) and W13 block scale is +0 or a normal power
+ *                    of two, as moe_quantize_act_1x128_ue8m0 and
+ *                    moe_requant_scales_ue8m0 produce.  The gate/up GEMM on
+ *                    the tensor-core tiles then hands the scales to the
+ *                    tensor core as UE8M0 scale factors
+ *                    (tcgen05.mma kind::mxf8f6f4.block_scale) and each tile
+ *                    accumulates over all of K in tensor memory, with no
+ *                    per-slice promotion; a scale that is not a power of two
+ *                    sets MOE_DEV_BAD_SCALE.  A zero scale becomes the
+ *                    smallest UE8M0 scale, 2^-127: its block adds at most
+ *                    about 2^-100 of the FP32 values it meets, and an expert
+ *                    whose W13 scales are all zero still yields exactly zero
+ *                    after SwiGLU (the products underflow).  The down GEMM,
+ *                    whose intermediate scales are amax/448, and the vector
+ *                    path keep the FP32 promotion.  Runs on single CTAs
+ *                    (MOE_TILE_PAIR then falls back to MOE_TILE_SINGLE).
+ * Any other value returns MOE_ERR_SHAPE. */
+#define MOE_SCALES_FP32 0
+#define MOE_SCALES_UE8M0 1
 
 /* Workspace bytes the forward needs (host-only; 0 for invalid sizes).  The
  * workspace holds the BF16 route contributions [M * top_k, H], for problems

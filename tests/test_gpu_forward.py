@@ -26,12 +26,12 @@ def _load():
     L.load()
 
 
-def _run(prob, debug=True, tile_mode=L.TILE_AUTO):
+def _run(prob, debug=True, tile_mode=L.TILE_AUTO, scale_mode=L.SCALES_FP32):
     cap = prob.sorted_ids.numel()
     dq = torch.zeros(cap, prob.cfg.I, dtype=torch.uint8, device="cuda") if debug else None
     ds = torch.zeros(cap, prob.cfg.I // 128, dtype=torch.float32, device="cuda") if debug else None
     prob.run_plan()
-    prob.run_forward(prob.fwd_args(dq, ds, tile_mode=tile_mode))
+    prob.run_forward(prob.fwd_args(dq, ds, tile_mode=tile_mode, scale_mode=scale_mode))
     torch.cuda.synchronize()
     return dq, ds
 
@@ -157,10 +157,10 @@ FULL = {
 MANY_BLOCKS = W.CONFIGS["prefill_8192"].with_(name="prefill_8192_bm64", block_m=64)
 
 
-def _full_size(name, tile_mode, cfg=None):
+def _full_size(name, tile_mode, cfg=None, scale_mode=L.SCALES_FP32):
     cfg = cfg or W.CONFIGS[name]
     prob = DeviceProblem(cfg)
-    dq, ds = _run(prob, tile_mode=tile_mode)
+    dq, ds = _run(prob, tile_mode=tile_mode, scale_mode=scale_mode)
     tokens = np.arange(cfg.M) if FULL.get(name, "blocks") is None else block_cover_tokens(prob)
     if name == "skewed":
         ids = prob.routing.topk_ids.numpy()
@@ -275,6 +275,43 @@ def test_forward_modes_agree(name, modes):
     assert torch.allclose(o1, o2, rtol=1e-2, atol=1e-2)
     nd, nf = code_diffs(q1, q2)
     assert nf == 0 and nd <= max(1, CODE_DIFF_FRAC * q1.size)
+
+
+# ------------------------------------------------------------------ hardware block scaling (UE8M0 scale factors)
+
+# Power-of-two scales on both operands: the gate/up GEMM applies them in the
+# tensor core.  Small cases split K; "bs_tiles" has enough tiles not to.
+BLOCK_SCALED = {
+    "ue8m0_both": SMALL["ue8m0_both"],
+    "bs_masked_zero": SMALL["masked_zero"].with_(name="bs_masked_zero", ue8m0=True, act_ue8m0=True),
+    "bs_ragged_bm8": SMALL["ragged_bm8"].with_(name="bs_ragged_bm8", ue8m0=True, act_ue8m0=True),
+    "bs_tiles": W.MoEConfig("bs_tiles", M=2048, H=512, I=512, E=32, top_k=4, block_m=128, ue8m0=True,
+                            act_ue8m0=True, out_init="normal0.1", routed_scale=2.5),
+}
+
+
+@pytest.mark.parametrize("name", list(BLOCK_SCALED))
+def test_forward_block_scaled_all_tokens(name):
+    prob = DeviceProblem(BLOCK_SCALED[name])
+    dq, ds = _run(prob, tile_mode=L.TILE_SINGLE, scale_mode=L.SCALES_UE8M0)
+    _check(prob, np.arange(prob.cfg.M), dq, ds, "block-scaled")
+    assert int(prob.status.item()) == 0
+
+
+def test_forward_block_scaled_full_size():
+    """The large workload (E257/H7168/I1024/top-9, UE8M0 weights) with UE8M0
+    activation scales too, on a token set covering every plan block."""
+    cfg = W.CONFIGS["large"].with_(name="large_act_ue8m0", act_ue8m0=True)
+    _full_size(cfg.name, L.TILE_AUTO, cfg, scale_mode=L.SCALES_UE8M0)
+
+
+@pytest.mark.parametrize("which", ["activations", "weights"])
+def test_forward_block_scaled_reports_scales_that_are_not_powers_of_two(which):
+    cfg = SMALL["ue8m0_both"].with_(name="bs_bad", act_ue8m0=(which != "activations"), ue8m0=(which != "weights"))
+    prob = DeviceProblem(cfg)
+    _run(prob, debug=False, tile_mode=L.TILE_SINGLE, scale_mode=L.SCALES_UE8M0)
+    assert int(prob.status.item()) & L.MOE_DEV_BAD_SCALE
+    assert torch.isfinite(prob.out.float()).all()
 
 
 # ------------------------------------------------------------------ semantics
