@@ -702,11 +702,11 @@ def extra_sweep(cfg, prob, flush, peaks):
     return out
 
 
-def measure_w4a8(M, flush, peaks, steps=5, warmup=3):
-    """moe_w4a8_forward (E2M1-K32 weights x per-row FP8 activations, the
-    CUDA-core path) at the SM120 page's timing shape E288/H4096/I1024/top-8
-    with plan blocks of 16 rows; the plan is built once and L2 is flushed
-    before each timed forward.  FLOP = Rv * 6 * H * I; bytes = the touched
+def measure_w4a8(M, flush, peaks, steps=5, warmup=3, path=0):
+    """moe_w4a8_forward (E2M1-K32 weights x per-row FP8 activations; path 0:
+    the tensor cores, 1: the CUDA cores) at the SM120 page's timing shape
+    E288/H4096/I1024/top-8 with plan blocks of 16 rows; the plan is built
+    once and L2 is flushed before each timed forward.  FLOP = Rv * 6 * H * I; bytes = the touched
     experts' packed codes and K32 scales (1.875 * H * I each) + activations,
     their row scales and `out` read and written."""
     import torch
@@ -715,7 +715,7 @@ def measure_w4a8(M, flush, peaks, steps=5, warmup=3):
     cfg = W.MoEConfig(f"w4a8_e288_m{M}", M=M, H=4096, I=1024, E=288, top_k=8, block_m=16)
     p = W4A8Problem(cfg)
     p.run_plan()
-    args = p.fwd_args()
+    args = p.fwd_args(path=path)
     for _ in range(warmup):
         p.run_forward(args)
     times = []
@@ -736,7 +736,8 @@ def measure_w4a8(M, flush, peaks, steps=5, warmup=3):
     nbytes = U * 1.875 * cfg.H * cfg.I + M * (cfg.H + 4) + 4 * M * cfg.H
     return {"M": M, "ms_forward": ms, "tflops": flop / (ms * 1e-3) / 1e12,
             "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "path": "CUDA cores (gate/up, requant, down, combine kernels and a flag memset)"}
+            "path": ("tensor cores (tcgen05 E2M1 x E4M3 projections; requant, combine kernels and a flag memset)"
+                     if path == 0 else "CUDA cores (gate/up, requant, down, combine kernels and a flag memset)")}
 
 
 def measure_router(M, E, k, flush, peaks, steps=20, warmup=5):
@@ -790,7 +791,9 @@ def main():
         L.load()
         peaks = load_peaks()
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        print(json.dumps({f"w4a8_e288_m{M}": measure_w4a8(M, flush, peaks) for M in (1, 1024)}), flush=True)
+        res = {f"w4a8_e288_m{M}": measure_w4a8(M, flush, peaks) for M in (1, 1024)}
+        res.update({f"w4a8_e288_m{M}_cuda_cores": measure_w4a8(M, flush, peaks, path=1) for M in (1, 1024)})
+        print(json.dumps(res), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3

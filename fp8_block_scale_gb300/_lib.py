@@ -65,6 +65,7 @@ class MoeFwdArgs(ctypes.Structure):
 
 
 TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_VECTOR = 0, 1, 2, 3
+W4A8_AUTO, W4A8_CUDA_CORES = 0, 1
 SCALES_FP32, SCALES_UE8M0 = 0, 1
 
 
@@ -96,6 +97,7 @@ class MoeW4A8Args(ctypes.Structure):
         ("top_k", ctypes.c_int32),
         ("block_m", ctypes.c_int32),
         ("routed_scale", ctypes.c_float),
+        ("path", ctypes.c_int32),
     ]
 
 

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_fp8.so")
-SOURCES = ["api.cu", "plan.cu", "prep.cu", "forward.cu", "vector.cu", "noalloc.cu", "router.cu", "w4a8.cu"]
+SOURCES = ["api.cu", "plan.cu", "prep.cu", "forward.cu", "vector.cu", "noalloc.cu", "router.cu", "w4a8.cu", "w4a8_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]

@@ -38,9 +38,9 @@ bool on_device(const void* p, int device) {
   return false;
 }
 
-CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                              CUtensorMapSwizzle swizzle) {
+CUresult encode_tensor_map_2d_typed(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                                    uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -56,9 +56,15 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                              CUtensorMapSwizzle swizzle) {
+  return encode_tensor_map_2d_typed(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, outer, row_stride_bytes,
+                                    box_inner, box_outer, swizzle);
 }
 
 }  // namespace moe

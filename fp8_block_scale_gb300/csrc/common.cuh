@@ -68,6 +68,10 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
 CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                               CUtensorMapSwizzle swizzle);
+// The same for another element type (sizes in elements, the stride in bytes).
+CUresult encode_tensor_map_2d_typed(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                                    uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 // ---------------------------------------------------------------- device side
 
@@ -301,6 +305,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+// Instruction descriptor, kind::f8f6f4: A E2M1 (FP4, in the padded shared-
+// memory form the copy engine writes for 16U4_ALIGN16B tensors) x B E4M3
+// -> F32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e2m1_e4m3_f32(int m, int n) {
+  return (1u << 4)                                 // D format F32
+         | (5u << 7) | (0u << 10)                  // A E2M1, B E4M3
+         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
+}
 
 // ---- FP8 conversion
 

@@ -3,8 +3,12 @@
 // description): E2M1 weight codes with one FP32 scale per 32 elements of K,
 // applied in FP32, and E4M3 activations with one FP32 scale per row.
 //
-// The projections run on the CUDA cores; each CTA of the first three kernels
-// takes one plan block (in the projections, and a group of columns):
+// Where the sizes allow (H and I multiples of 128, plan blocks of at most 64
+// rows), the two projections run on the tensor cores (w4a8_tc.cu) and the
+// requant and combine kernels below complete the forward.  Otherwise, or on
+// request (MOE_W4A8_CUDA_CORES), the projections run on the CUDA cores; each
+// CTA of the first three kernels takes one plan block (in the projections,
+// and a group of columns):
 //   w4a8_up_kernel       gate/up rows of the block's expert against the block's
 //                        activation rows (staged in shared memory), SwiGLU;
 //   w4a8_requant_kernel  each route's SwiGLU row requantised to E4M3 with one
@@ -18,6 +22,7 @@
 // one scale per block, the codes decoded once per chunk of kRowChunk rows,
 // whose partial sums stay in registers until a warp reduction.
 #include "common.cuh"
+#include "w4a8_tc.cuh"
 #include "../../include/moe_w4a8.h"
 
 namespace moe {
@@ -508,6 +513,7 @@ moe_status moe_w4a8_forward(const moe_w4a8_args* a, moe_stream_t stream) {
   if (a->M < 0 || a->H < 32 || a->H % 32 || a->I < 32 || a->I % 32 || a->E < 1 || a->top_k < 1 || a->top_k > 64)
     return MOE_ERR_SHAPE;
   if (a->block_m < 8 || a->block_m > kW4MaxBlockM || a->block_m % 8) return MOE_ERR_SHAPE;
+  if (a->path != MOE_W4A8_AUTO && a->path != MOE_W4A8_CUDA_CORES) return MOE_ERR_SHAPE;
   if (static_cast<int64_t>(a->block_m) * a->H > kW4MaxRowBytes ||
       static_cast<int64_t>(a->block_m) * a->I > kW4MaxRowBytes)
     return MOE_ERR_SHAPE;
@@ -549,6 +555,51 @@ moe_status moe_w4a8_forward(const moe_w4a8_args* a, moe_stream_t stream) {
   const unsigned nblocks = static_cast<unsigned>(a->blocks_cap);
 
   MOE_CUDA_TRY(cudaMemsetAsync(rvalid, 0, static_cast<size_t>(R) * 4, stream));
+  const bool tc = a->path == MOE_W4A8_AUTO &&
+                  w4a8_tc_supported(a->H, a->I, a->block_m, a->w13, a->w2, a->w13_scale, a->w2_scale);
+  if (tc) {
+    W4GemmParams gp{};
+    gp.sorted_ids = a->sorted_token_ids;
+    gp.expert_ids = a->expert_ids;
+    gp.num_post_padded = a->num_tokens_post_padded;
+    gp.status = a->device_status;
+    gp.nblocks = a->blocks_cap;
+    gp.R = static_cast<int>(R);
+    gp.top_k = a->top_k;
+    gp.block_m = a->block_m;
+    gp.E = a->E;
+    gp.H = a->H;
+    gp.I = a->I;
+    gp.routed_scale = a->routed_scale;
+    W4GemmParams gu = gp;
+    gu.up = 1;
+    gu.a_scale = a->a_scale;
+    gu.h = h;
+    gu.ntw = a->I / 64;
+    gu.w_rows = 2 * a->I;
+    const W4GemmTensors tu{a->w13, a->w13_scale, static_cast<uint64_t>(a->E) * 2 * a->I, a->a,
+                           static_cast<uint64_t>(a->M), static_cast<uint64_t>(a->H)};
+    moe_status st = launch_w4a8_tc_gemm(tu, gu, dev.sms, stream);
+    if (st != MOE_OK) return st;
+    const W4RequantParams rq{pl, h, q, s, rvalid, a->debug_q_inter, a->debug_s_inter, a->I};
+    w4a8_requant_kernel<<<nblocks, kW4Threads, 0, stream>>>(rq);
+    MOE_CUDA_TRY(cudaGetLastError());
+    W4GemmParams gd = gp;
+    gd.up = 0;
+    gd.s_inter = s;
+    gd.topk_w = a->topk_weights;
+    gd.y = y;
+    gd.ntw = a->H / 128;
+    gd.w_rows = a->H;
+    const W4GemmTensors td{a->w2, a->w2_scale, static_cast<uint64_t>(a->E) * a->H, q, static_cast<uint64_t>(R),
+                           static_cast<uint64_t>(a->I)};
+    st = launch_w4a8_tc_gemm(td, gd, dev.sms, stream);
+    if (st != MOE_OK) return st;
+    w4a8_combine_kernel<<<dim3(static_cast<unsigned>(a->M), static_cast<unsigned>(ceil_div(a->H, 4 * kW4Threads))),
+                          kW4Threads, 0, stream>>>(a->out, y, rvalid, a->H, a->top_k);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+  }
   const W4UpParams up{pl, a->a, a->a_scale, a->w13, a->w13_scale, h, a->device_status, a->H, a->I};
   w4a8_up_kernel<<<dim3(nblocks, static_cast<unsigned>(a->I / kUpCols)), kW4Threads,
                    static_cast<size_t>(a->block_m) * a->H, stream>>>(up);

@@ -170,11 +170,13 @@ class W4A8Problem:
         L.moe_plan(self.topk_ids, self.cfg.E, self.cfg.block_m, self.sorted_ids, self.expert_ids, self.ntpp,
                    self.plan_ws, stream)
 
-    def fwd_args(self, debug_q=None, debug_s=None, out=None):
-        return L.make_w4a8_args(self.a, self.a_scale, self.w13, self.w13_scale, self.w2, self.w2_scale,
+    def fwd_args(self, debug_q=None, debug_s=None, out=None, path=L.W4A8_AUTO):
+        args = L.make_w4a8_args(self.a, self.a_scale, self.w13, self.w13_scale, self.w2, self.w2_scale,
                                 self.topk_weights, self.sorted_ids, self.expert_ids, self.ntpp,
                                 self.out if out is None else out, self.workspace, self.cfg.top_k,
                                 self.cfg.block_m, self.cfg.routed_scale, self.status, debug_q, debug_s)
+        args.path = path
+        return args
 
     def run_forward(self, args=None, stream=None):
         L.moe_w4a8_forward(self.fwd_args() if args is None else args, stream)

@@ -69,8 +69,13 @@ moe_status moe_quantize_weight_k32(const uint16_t* w, int64_t rows, int K, uint8
  * blocks whose expert is -1 contribute nothing; any other expert id outside
  * [0, E) sets MOE_DEV_BAD_EXPERT and its block is skipped.
  *
- * This entry point runs the projections on the CUDA cores (four kernels and a
- * memset of the route flags); the workspace needs no initialisation.
+ * The projections run on the tensor cores (tcgen05 kind::f8f6f4, E2M1 x E4M3
+ * into tensor memory, each 32-wide K block promoted in FP32 with its weight
+ * row's scale) when H and I are multiples of 128, block_m <= 64, w13 and w2
+ * are 32-byte aligned and the scale arrays 16-byte aligned; otherwise, or
+ * with path = MOE_W4A8_CUDA_CORES, on the CUDA cores.  Five launches either
+ * way (a memset of the route flags, gate/up, requant, down, combine); the
+ * workspace needs no initialisation.
  * ------------------------------------------------------------------------ */
 typedef struct moe_w4a8_args {
   const uint8_t* a;                        /* [M, H] E4M3 activations                       */
@@ -98,7 +103,15 @@ typedef struct moe_w4a8_args {
   int32_t top_k;
   int32_t block_m;
   float routed_scale;                      /* routed scaling factor (1.0 = none)            */
+  int32_t path;                            /* MOE_W4A8_AUTO or MOE_W4A8_CUDA_CORES          */
 } moe_w4a8_args;
+
+/* path values: MOE_W4A8_AUTO (0) takes the tensor cores where the sizes and
+ * alignments allow; MOE_W4A8_CUDA_CORES (1) always runs the projections on
+ * the CUDA cores.  Both compute the same result up to FP32 summation order.
+ * Any other value returns MOE_ERR_SHAPE. */
+#define MOE_W4A8_AUTO 0
+#define MOE_W4A8_CUDA_CORES 1
 
 /* Workspace bytes of the forward (host-only; 0 for invalid sizes): route
  * flags [M * top_k], SwiGLU rows [M * top_k, I] FP32, their codes and row

@@ -61,12 +61,12 @@ def test_quantize_weight_k32_bit_exact():
     assert s[1, 2, 2].item() == 1.0
 
 
-def _run(prob, debug=True):
+def _run(prob, debug=True, path=L.W4A8_AUTO):
     cap = prob.sorted_ids.numel()
     dq = torch.zeros(cap, prob.cfg.I, dtype=torch.uint8, device="cuda") if debug else None
     ds = torch.zeros(cap, dtype=torch.float32, device="cuda") if debug else None
     prob.run_plan()
-    prob.run_forward(prob.fwd_args(dq, ds))
+    prob.run_forward(prob.fwd_args(dq, ds, path=path))
     torch.cuda.synchronize()
     return dq, ds
 
@@ -112,13 +112,25 @@ CASES = {
                                     out_init="normal0.1", garbage_plan=True),
     "w4a8_skewed": W.MoEConfig("w4a8_skewed", M=96, H=256, I=256, E=16, top_k=4, block_m=16, routing="skewed",
                                masked_frac=0.05, n_hot=2, hot_frac=0.5, n_zero_scale=1),
+    # shapes the tensor-core projections take (H, I multiples of 128): groups
+    # of 8 blocks of 8 rows, groups of two 24-row blocks (48 columns), single
+    # 64-row blocks over a garbage-filled plan
+    "w4a8_tc_bm8": W.MoEConfig("w4a8_tc_bm8", M=37, H=384, I=256, E=5, top_k=3, block_m=8, routed_scale=2.5,
+                               masked_frac=0.1, id_dtype=torch.int64),
+    "w4a8_tc_bm24": W.MoEConfig("w4a8_tc_bm24", M=120, H=256, I=128, E=6, top_k=2, block_m=24, routing="skewed",
+                                n_hot=1, hot_frac=0.6, out_init="normal0.1"),
+    "w4a8_tc_bm64": W.MoEConfig("w4a8_tc_bm64", M=200, H=512, I=384, E=6, top_k=4, block_m=64,
+                                out_init="normal0.1", garbage_plan=True),
 }
 
 
+@pytest.mark.parametrize("path", [L.W4A8_AUTO, L.W4A8_CUDA_CORES], ids=["auto", "cuda_cores"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_w4a8_forward_small(name):
+def test_w4a8_forward_small(name, path):
+    """Every case on the automatic choice (the tensor cores where H and I are
+    multiples of 128) and on the CUDA cores."""
     prob = W4A8Problem(CASES[name])
-    dq, ds = _run(prob)
+    dq, ds = _run(prob, path=path)
     _check(prob, np.arange(prob.cfg.M), dq, ds)
 
 
