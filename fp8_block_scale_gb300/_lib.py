@@ -13,6 +13,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_fp8.so")
+LIB_DEBUG_PATH = os.path.join(_PKG, "libmoe_fp8_debug.so")  # the bounds-checking build
 
 MOE_OK = 0
 STATUS_NAMES = {
@@ -101,7 +102,8 @@ class MoeW4A8Args(ctypes.Structure):
     ]
 
 
-_lib = None
+_libs = {}
+_active = LIB_PATH
 
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -138,14 +140,21 @@ _SIGS = {
                                                ctypes.c_void_p, ctypes.c_void_p]),
     "moe_w4a8_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "moe_w4a8_forward": (ctypes.c_int, [ctypes.POINTER(MoeW4A8Args), ctypes.c_void_p]),
+    "moe_debug_bounds_enabled": (ctypes.c_int, []),
+    "moe_debug_bounds_selftest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                 ctypes.c_void_p]),
+    "moe_debug_bounds_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_char_p),
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.c_int]),
 }
 
 
-def load(path=LIB_PATH):
-    """Load libmoe_fp8.so (built by ``fp8_block_scale_gb300.build.build()``)."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def load(path=None):
+    """Load the library the wrappers call (libmoe_fp8.so unless ``use_library``
+    selected another), built by ``fp8_block_scale_gb300.build.build()``."""
+    path = _active if path is None else path
+    lib = _libs.get(path)
+    if lib is not None:
+        return lib
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
     lib = ctypes.CDLL(path)
@@ -153,8 +162,49 @@ def load(path=LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _libs[path] = lib
     return lib
+
+
+class use_library:
+    """Context manager: the wrappers call the library at `path` (for example
+    LIB_DEBUG_PATH, the bounds-checking build) inside the block."""
+
+    def __init__(self, path):
+        self.path = path
+        self.prev = None
+
+    def __enter__(self):
+        global _active
+        load(self.path)
+        self.prev, _active = _active, self.path
+        return _libs[self.path]
+
+    def __exit__(self, *exc):
+        global _active
+        _active = self.prev
+        return False
+
+
+def moe_debug_bounds_enabled():
+    return bool(load().moe_debug_bounds_enabled())
+
+
+def moe_debug_bounds_selftest(data, probe, out, stream=None):
+    """Read data[probe] into out[0] through the bounds checks (int32 device tensors)."""
+    _check("moe_debug_bounds_selftest", load().moe_debug_bounds_selftest(
+        _ptr(data), data.numel(), int(probe), _ptr(out), _stream(stream)))
+
+
+def moe_debug_bounds_read(reset=False):
+    """(failures, first_file, first_line) of the active library's bounds
+    checks since the last reset; waits for the device first."""
+    n = ctypes.c_uint64()
+    f = ctypes.c_char_p()
+    line = ctypes.c_int32()
+    _check("moe_debug_bounds_read", load().moe_debug_bounds_read(ctypes.byref(n), ctypes.byref(f),
+                                                                 ctypes.byref(line), 1 if reset else 0))
+    return n.value, (f.value.decode() if f.value else None), line.value
 
 
 def _ptr(t):

@@ -2,7 +2,9 @@
 // queries, tensor-map encoding, plan capacity and workspace helpers.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -67,9 +69,74 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner
                                     box_inner, box_outer, swizzle);
 }
 
+// Readers of the translation units' bounds records (registered while the
+// library loads; empty in the normal build).
+namespace {
+struct BoundsEntry {
+  BoundsReader reader;
+  const char* file;
+};
+std::vector<BoundsEntry>& bounds_registry() {
+  static std::vector<BoundsEntry> v;
+  return v;
+}
+}  // namespace
+
+void bounds_register(BoundsReader reader, const char* file) { bounds_registry().push_back({reader, file}); }
+
+// Self-test of the bounds checks: reads data[probe] into *out only when the
+// check passes (-1 otherwise).
+__global__ void bounds_selftest_kernel(const int32_t* data, int n, int probe, int32_t* out) {
+  int32_t v = -1;
+  if (MOE_IN_BOUNDS(probe >= 0 && probe < n)) v = data[probe];
+  *out = v;
+}
+
 }  // namespace moe
 
 extern "C" {
+
+int moe_debug_bounds_enabled(void) {
+#ifdef MOE_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+moe_status moe_debug_bounds_selftest(const int32_t* data, int n, int probe, int32_t* out, moe_stream_t stream) {
+  using namespace moe;
+  if (!data || !out) return MOE_ERR_NULL;
+  if (n < 1) return MOE_ERR_SHAPE;
+  // without the device-side checks an out-of-range probe is refused here
+  if (!moe_debug_bounds_enabled() && (probe < 0 || probe >= n)) return MOE_ERR_SHAPE;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if (!on_device(data, dev.device) || !on_device(out, dev.device)) return MOE_ERR_DEVICE;
+  bounds_selftest_kernel<<<1, 1, 0, stream>>>(data, n, probe, out);
+  MOE_CUDA_TRY(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status moe_debug_bounds_read(uint64_t* failures, const char** first_file, int32_t* first_line, int reset) {
+  if (!failures) return MOE_ERR_NULL;
+  *failures = 0;
+  if (first_file) *first_file = nullptr;
+  if (first_line) *first_line = 0;
+  if (moe::bounds_registry().empty()) return MOE_OK;
+  MOE_CUDA_TRY(cudaDeviceSynchronize());
+  for (const auto& entry : moe::bounds_registry()) {
+    moe::BoundsRecord r = {};
+    MOE_CUDA_TRY(entry.reader(&r, reset));
+    if (r.failures != 0 && *failures == 0) {
+      const char* base = std::strrchr(entry.file, '/');
+      if (first_file) *first_file = base ? base + 1 : entry.file;
+      if (first_line) *first_line = r.first_line;
+    }
+    *failures += r.failures;
+  }
+  return MOE_OK;
+}
 
 const char* moe_status_string(int status) {
   switch (status) {
@@ -106,3 +173,5 @@ moe_status moe_workspace_init(void* workspace, size_t bytes, moe_stream_t stream
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

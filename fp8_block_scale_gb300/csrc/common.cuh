@@ -73,6 +73,66 @@ CUresult encode_tensor_map_2d_typed(CUtensorMap* map, CUtensorMapDataType dtype,
                                     uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                                     uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// ---------------------------------------------------------------- bounds checks
+//
+// MOE_IN_BOUNDS(c) guards a global access or a tensor copy whose index is
+// derived from data (plan entries, route and token ids, expert ids) or from
+// tiling arithmetic.  In a library built with -DMOE_DEBUG_BOUNDS it counts a
+// failed check in this translation unit's bounds record (and keeps the first
+// failing source line), then returns false: the caller skips the access, or
+// moves a tensor copy to coordinate 0 so that its barrier still receives the
+// bytes it expects.  Nothing traps.  In the normal build it is the constant
+// true and the checks compile away.  Each translation unit ends with
+// MOE_BOUNDS_TU(), which registers a host reader of its record for
+// moe_debug_bounds_read.
+struct BoundsRecord {
+  unsigned long long failures;
+  int first_line;
+  int pad;
+};
+using BoundsReader = cudaError_t (*)(BoundsRecord* out, int reset);
+void bounds_register(BoundsReader reader, const char* file);
+
+#ifdef MOE_DEBUG_BOUNDS
+static __device__ BoundsRecord g_bounds;
+__device__ __forceinline__ bool bounds_note(bool ok, int line) {
+  if (!ok) {
+    atomicAdd(&g_bounds.failures, 1ull);
+    atomicCAS(&g_bounds.first_line, 0, line);
+  }
+  return ok;
+}
+#define MOE_IN_BOUNDS(c) ::moe::bounds_note(static_cast<bool>(c), __LINE__)
+#define MOE_BOUNDS_TU()                                                                      \
+  namespace {                                                                                \
+  cudaError_t bounds_read_tu(::moe::BoundsRecord* out, int reset) {                          \
+    cudaError_t err = cudaMemcpyFromSymbol(out, ::moe::g_bounds, sizeof(::moe::BoundsRecord)); \
+    if (err == cudaSuccess && reset) {                                                       \
+      const ::moe::BoundsRecord zero = {};                                                   \
+      err = cudaMemcpyToSymbol(::moe::g_bounds, &zero, sizeof(zero));                        \
+    }                                                                                        \
+    return err;                                                                              \
+  }                                                                                          \
+  const bool bounds_registered_tu = (::moe::bounds_register(bounds_read_tu, __FILE__), true); \
+  }
+#else
+#define MOE_IN_BOUNDS(c) true
+#define MOE_BOUNDS_TU()
+#endif
+
+// A 2D tensor copy's coordinates: the innermost one (x, in elements) a
+// multiple of `x_align` (16 bytes' worth) and inside the row, the outer one
+// inside the tensor.  A failing copy is moved to the origin, which every
+// tensor the library copies from has.
+#define MOE_CHECK_BOX(x, y, x_extent, y_extent, x_align)                                               \
+  do {                                                                                                 \
+    if (!MOE_IN_BOUNDS((x) >= 0 && (x) % (x_align) == 0 && static_cast<int64_t>(x) < (x_extent) &&     \
+                       (y) >= 0 && static_cast<int64_t>(y) < (y_extent))) {                            \
+      (x) = 0;                                                                                         \
+      (y) = 0;                                                                                         \
+    }                                                                                                  \
+  } while (0)
+
 // ---------------------------------------------------------------- device side
 
 // A bounded wait gives up after this long (the whole forward takes well under

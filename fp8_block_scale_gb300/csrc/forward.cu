@@ -164,6 +164,8 @@ struct GemmParams {
   float* usum;                 // up, splits > 1: [nblocks, ntiles_n, block_m, 256] zeroed partial sums
   int32_t* ucnt;               // up, splits > 1: [nblocks, ntiles_n] zeroed arrival tickets
   uint32_t* gen;               // up: forward stamp, advanced once per forward
+  int64_t a_rows;              // rows of the A operand's tensor (M tokens, or sorted_cap plan slots)
+  int64_t q_rows;              // up: rows of q_inter (sorted_cap)
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -184,7 +186,8 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
 }
 
 __device__ __forceinline__ int block_expert(const GemmParams& p, const SmemCtl* ctl, int64_t b) {
-  return b < kMaxBlocksSmem ? ctl->expert[b] : p.expert_ids[b];
+  if (b < kMaxBlocksSmem) return ctl->expert[b];
+  return MOE_IN_BOUNDS(b < p.nblocks) ? p.expert_ids[b] : -1;
 }
 
 // Tile -> (plan block, n tile, K split, expert); false if the tile has no
@@ -214,7 +217,8 @@ __device__ __forceinline__ void load_ids(const GemmParams& p, int b, int lane, i
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 4 * lane + i;
-    id[i] = r < p.block_m ? p.sorted_ids[static_cast<int64_t>(b) * p.block_m + r] : -1;
+    const int64_t q = static_cast<int64_t>(b) * p.block_m + r;
+    id[i] = (r < p.block_m && MOE_IN_BOUNDS(q < p.nblocks * p.block_m)) ? p.sorted_ids[q] : -1;
   }
 }
 
@@ -393,7 +397,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (lane == 0) {
           const uint32_t full = smem_u32(&ctl->full[npre]);
           mbar_expect_tx(full, kBStage);
-          tma_load_2d(smem_u32(sB + npre * kBStage), &tmB, full, pkb * kTileK, pe * p.b_rows + pt_n * kTileN);
+          int bx = pkb * kTileK, by = pe * p.b_rows + pt_n * kTileN;
+          MOE_CHECK_BOX(bx, by, p.nkb * kTileK, static_cast<int64_t>(p.E) * p.b_rows, 16);
+          tma_load_2d(smem_u32(sB + npre * kBStage), &tmB, full, bx, by);
         }
         ++npre;
         if (++pkb >= pkb1) {
@@ -426,6 +432,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const bool route = ids[i] >= 0 && ids[i] < p.R;
           mine |= route;
           tok[i] = route ? ids[i] / p.top_k : 0;
+          if (!MOE_IN_BOUNDS(tok[i] < p.a_rows)) tok[i] = 0;
         }
         // only groups with a route are fetched; the other rows keep stale
         // shared memory, whose products land in rows the epilogue ignores
@@ -459,29 +466,40 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // they would land last and hold up the epilogue, which frees the stage
         if (lane == 0) {
           StageExtra* x = sX + s;
-          bulk_load(smem_u32(x->a_scale), p.a_scale_t + kb * p.cap_pad + slot0, 512u, xfull);
-          bulk_load(smem_u32(&x->w_scale), p.w_scale_st + (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb, 16u,
-                    xfull);
+          // (a failing check reads from offset 0 instead, so the stage still completes)
+          const bool slots_ok = MOE_IN_BOUNDS(slot0 >= 0 && slot0 % 4 == 0 && slot0 + 128 <= p.cap_pad);
+          int64_t as_off = static_cast<int64_t>(kb) * p.cap_pad + slot0;
+          if (!slots_ok || !MOE_IN_BOUNDS(kb < p.nkb)) as_off = 0;
+          int64_t ws_off = (static_cast<int64_t>(b) * p.ntiles_n + t) * p.nkb + kb;
+          if (!MOE_IN_BOUNDS(ws_off < p.nblocks * p.ntiles_n * p.nkb)) ws_off = 0;
+          bulk_load(smem_u32(x->a_scale), p.a_scale_t + as_off, 512u, xfull);
+          bulk_load(smem_u32(&x->w_scale), p.w_scale_st + ws_off, 16u, xfull);
           if (tile_info) {
-            bulk_load(smem_u32(x->tok), p.slot_route + slot0, 512u, xfull);
-            bulk_load(smem_u32(x->weight), p.slot_w + slot0, 512u, xfull);
+            bulk_load(smem_u32(x->tok), p.slot_route + (slots_ok ? slot0 : 0), 512u, xfull);
+            bulk_load(smem_u32(x->weight), p.slot_w + (slots_ok ? slot0 : 0), 512u, xfull);
           }
         }
         __syncwarp();
         const uint32_t a_dst = smem_u32(sA + s * kABytes);
         if (kUp && !kPair && p.a_gather4) {
-          if (mine) tma_gather4(a_dst + 512u * lane, &tmA, full, kb * kTileK, tok[0], tok[1], tok[2], tok[3]);
+          int gx = kb * kTileK, gy = 0;
+          MOE_CHECK_BOX(gx, gy, p.nkb * kTileK, 1, 16);
+          if (mine) tma_gather4(a_dst + 512u * lane, &tmA, full, gx, tok[0], tok[1], tok[2], tok[3]);
         } else if (lane == 0 && has_rows) {
+          int ax = kb * kTileK, ay = mb * p.block_m;
+          MOE_CHECK_BOX(ax, ay, p.nkb * kTileK, p.a_rows, 16);
           if (kPair)
-            tma_load_2d_pair(a_dst, &tmA, full, kb * kTileK, mb * p.block_m);
+            tma_load_2d_pair(a_dst, &tmA, full, ax, ay);
           else
-            tma_load_2d(a_dst, &tmA, full, kb * kTileK, mb * p.block_m);
+            tma_load_2d(a_dst, &tmA, full, ax, ay);
         }
         if (lane == 0 && !pre) {
+          int bx = kb * kTileK, by = brow;
+          MOE_CHECK_BOX(bx, by, p.nkb * kTileK, static_cast<int64_t>(p.E) * p.b_rows, 16);
           if (kPair)
-            tma_load_2d_pair(smem_u32(sB + s * kBStage), &tmB, full, kb * kTileK, brow);
+            tma_load_2d_pair(smem_u32(sB + s * kBStage), &tmB, full, bx, by);
           else
-            tma_load_2d(smem_u32(sB + s * kBStage), &tmB, full, kb * kTileK, brow);
+            tma_load_2d(smem_u32(sB + s * kBStage), &tmB, full, bx, by);
         }
         ++it;
       }
@@ -667,7 +685,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (ok && lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
         if (p.splits > 1) {
           const int64_t slot = static_cast<int64_t>(b) * p.block_m + row;
-          ctl->row_tok[row] = row < p.block_m ? p.slot_route[slot] : -1;
+          ctl->row_tok[row] = (row < p.block_m && MOE_IN_BOUNDS(slot < p.cap_pad)) ? p.slot_route[slot] : -1;
         }
       }
       for (int kb = kb0; kb < (kBS ? kb0 : kb1); ++kb) {
@@ -741,10 +759,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // Every split takes its ticket, even one whose waits ran out (it adds
         // nothing then), and the last one clears all the tile's rows, so the
         // tickets and sums are back to zero after any forward.
-        const bool live = ok && MOE_RVALID && ctl->row_tok[row] >= 0;
-        float* srow = p.usum + ((static_cast<int64_t>(b) * p.ntiles_n + t) * p.block_m + (MOE_RVALID ? row : 0)) *
-                                   kTileN +
-                      128 * half;
+        const int64_t sum_row = (static_cast<int64_t>(b) * p.ntiles_n + t) * p.block_m + (MOE_RVALID ? row : 0);
+        const bool sum_ok = MOE_IN_BOUNDS(sum_row < p.nblocks * p.ntiles_n * p.block_m);
+        const bool live = ok && sum_ok && MOE_RVALID && ctl->row_tok[row] >= 0;
+        float* srow = p.usum + (sum_ok ? sum_row : 0) * kTileN + 128 * half;
         if (live) {
 #pragma unroll
           for (int c = 0; c < 128; c += 4) red_add_v4(srow + c, acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
@@ -752,7 +770,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __threadfence();
         named_barrier(1, 32 * kNumEpiWarps);
         if (warp == 2 && lane == 0) {
-          int32_t* cnt = p.ucnt + static_cast<int64_t>(b) * p.ntiles_n + t;
+          int64_t cnt_off = static_cast<int64_t>(b) * p.ntiles_n + t;
+          if (!MOE_IN_BOUNDS(cnt_off < p.nblocks * p.ntiles_n)) cnt_off = 0;
+          int32_t* cnt = p.ucnt + cnt_off;
           const int old = atomicAdd(cnt, 1);
           const bool last = old == p.splits - 1;
           if (last) *cnt = 0;
@@ -762,7 +782,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         have = ctl->last_flag != 0;
         if (have) {
           __threadfence();
-          if (MOE_RVALID) {
+          if (MOE_RVALID && sum_ok) {
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
               const float4 v = __ldcg(reinterpret_cast<const float4*>(srow + c));
@@ -795,7 +815,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // h / s as h * (1/s): the two roundings can move a value across an
         // E4M3 rounding midpoint only when it lies within an ulp of it
         const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-        if (ok && MOE_RVALID) {
+        if (ok && MOE_RVALID && MOE_IN_BOUNDS(MOE_SLOT < p.q_rows && MOE_SLOT < p.cap_pad)) {
           const int64_t slot = MOE_SLOT;
           uint32_t packed[16];
 #pragma unroll
@@ -846,7 +866,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const uint32_t* src = &buf[8 * i + sub][4 * c16];
                 uint4* dst = reinterpret_cast<uint4*>(p.y_out + static_cast<int64_t>(rts[i]) * p.H + hblk * 128 +
                                                       32 * ch + 8 * c16);
-                *dst = make_uint4(src[0], src[1], src[2], src[3]);
+                if (MOE_IN_BOUNDS(rts[i] < p.R && hblk * 128 + 32 * ch + 8 * c16 + 8 <= p.H))
+                  *dst = make_uint4(src[0], src[1], src[2], src[3]);
               }
             }
             __syncwarp();
@@ -892,6 +913,7 @@ struct StageParams {
   const uint32_t* gen;        // stamp of the previous forward (this one's is gen + 1)
   float* slot_w;              // [cap_pad]
   int32_t* status;            // nullable
+  int64_t a_rows;             // rows of a_sorted (sorted_cap)
   int check_pow2;             // block-scaled mode: activation scales must be +0 or normal powers of two
   float4* wsu;                // [nblocks, I/128, H/128]
   float4* wsd;                // [nblocks, ceil(H/256), I/128]
@@ -918,6 +940,7 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   const int nkb = p.H / 128, nib = p.I / 128;
   const int chunks = p.H / 16;
   for (int64_t slot = gtid / 32; slot < nslots; slot += nwarps) {
+    if (!MOE_IN_BOUNDS(slot < p.cap_pad)) break;
     const int id = p.sorted_ids[slot];
     const bool route = id >= 0 && id < p.R;
     const int64_t tok = route ? id / p.top_k : 0;
@@ -932,7 +955,7 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
       p.as_t[k * p.cap_pad + slot] = v;
       if (p.check_pow2 && !ue8m0_ok(v)) report(p.status, MOE_DEV_BAD_SCALE);
     }
-    if (p.a_sorted) {
+    if (p.a_sorted && MOE_IN_BOUNDS(slot < p.a_rows)) {
       // up to 4 KB of the row in flight per warp (8 loads per lane) before the stores
       const uint4* src = reinterpret_cast<const uint4*>(p.a + tok * p.H);
       uint4* dst = reinterpret_cast<uint4*>(p.a_sorted + slot * p.H);
@@ -959,6 +982,7 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
   const int per_block = up_items + dn_items;
   const int nrb13 = 2 * p.I / 128, nrb2 = p.H / 128;
   for (int64_t b = blockIdx.x; b < nvalid; b += gridDim.x) {
+    if (!MOE_IN_BOUNDS(b < p.nblocks)) break;
     const int e = p.expert_ids[b];
     if (e < 0 || e >= p.E) continue;
     for (int j = threadIdx.x; j < per_block; j += blockDim.x) {
@@ -1391,6 +1415,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     sp.I = a->I;
     sp.routed_scale = a->routed_scale;
     sp.status = a->device_status;
+    sp.a_rows = a->sorted_cap;
     sp.check_pow2 = block_scaled ? 1 : 0;
     int64_t sgrid = ceil_div(nblocks * a->block_m, 8);
     if (sgrid > static_cast<int64_t>(dev.sms) * 8) sgrid = static_cast<int64_t>(dev.sms) * 8;
@@ -1410,6 +1435,8 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     p.E = a->E;
     p.I = a->I;
     p.H = a->H;
+    p.q_rows = a->sorted_cap;
+    p.a_rows = a->sorted_cap;
 
     GemmParams up = p;
     up.a_scale_t = as_t;
@@ -1422,6 +1449,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     up.ntiles_n = N / kTileN;
     up.b_rows = N;
     up.a_gather4 = wl.pregather ? 0 : 1;
+    if (!wl.pregather) up.a_rows = a->M;
     up.tile_group = 0;
     up.slot_route = slot_route;
     up.gen = gen;
@@ -1510,3 +1538,5 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

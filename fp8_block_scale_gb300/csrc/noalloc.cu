@@ -63,3 +63,5 @@ moe_status moe_fp8_block_scale_forward_noalloc(const moe_fwd_args* args, moe_str
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

@@ -32,6 +32,8 @@ struct PlanWs {
   int32_t* rank;    // [R] stable rank of each route inside its chunk (or -1)
   int32_t* seg;     // [E] segment start of each expert
   int nchunks;
+  int64_t sorted_cap;  // entries of sorted_token_ids
+  int64_t blocks_cap;  // entries of expert_ids
 };
 
 __device__ __forceinline__ int load_id(const void* ids, int id_bits, int64_t r, int E) {
@@ -108,15 +110,17 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem /* 32 ints */) 
 // Pad sentinels (R) after each expert's routes and the expert of each of its
 // blocks: a warp per expert, lanes over the slots.
 __device__ void fill_pads(int E, int block_m, int64_t R, const int* totals, const int* seg, int32_t* sorted_ids,
-                          int32_t* expert_ids) {
+                          int32_t* expert_ids, int64_t sorted_cap, int64_t blocks_cap) {
   const int lane = threadIdx.x % 32;
   for (int e = threadIdx.x / 32; e < E; e += blockDim.x / 32) {
     const int tot = totals[e];
     if (tot == 0) continue;  // no routes: no slots, no blocks
     const int st = seg[e];
     const int end = st + (tot + block_m - 1) / block_m * block_m;
-    for (int q = st + tot + lane; q < end; q += 32) sorted_ids[q] = static_cast<int32_t>(R);
-    for (int b = st / block_m + lane; b < end / block_m; b += 32) expert_ids[b] = e;
+    for (int q = st + tot + lane; q < end; q += 32)
+      if (MOE_IN_BOUNDS(q >= 0 && q < sorted_cap)) sorted_ids[q] = static_cast<int32_t>(R);
+    for (int b = st / block_m + lane; b < end / block_m; b += 32)
+      if (MOE_IN_BOUNDS(b >= 0 && b < blocks_cap)) expert_ids[b] = e;
   }
 }
 
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(int64_t R, int 
     start += padded[i];
   }
   __syncthreads();
-  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids);
+  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids, ws.sorted_cap, ws.blocks_cap);
   if (threadIdx.x == 0) *num_post_padded = P;
 }
 
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, i
   if (rk < 0) return;
   const int e = load_id(ids, id_bits, r, E);
   const int base = ws.seg[e] + ws.counts[static_cast<int64_t>(e) * ws.nchunks + blockIdx.x];
-  sorted_ids[base + rk] = static_cast<int32_t>(r);
+  if (MOE_IN_BOUNDS(base + rk >= 0 && base + rk < ws.sorted_cap)) sorted_ids[base + rk] = static_cast<int32_t>(r);
 }
 
 // The whole plan in one CTA for R <= kSmallRoutes and E <= kSmallMaxExperts:
@@ -220,7 +224,8 @@ __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, i
 // three-launch path (a stable counting sort).
 __global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* ids, int id_bits, int64_t R, int E,
                                                                    int block_m, int32_t* sorted_ids,
-                                                                   int32_t* expert_ids, int32_t* num_post_padded) {
+                                                                   int32_t* expert_ids, int32_t* num_post_padded,
+                                                                   int64_t sorted_cap, int64_t blocks_cap) {
   extern __shared__ int32_t wh[];  // [32][E]: per-warp counts, then their exclusive prefix over warps
   __shared__ int scan_smem[33];
   __shared__ int totals[kSmallMaxExperts];
@@ -269,8 +274,11 @@ __global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* id
   }
   if (threadIdx.x == 0) *num_post_padded = P;
   __syncthreads();
-  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids);
-  if (e >= 0) sorted_ids[seg[e] + wh[warp * E + e] + in_warp] = static_cast<int32_t>(r);
+  fill_pads(E, block_m, R, totals, seg, sorted_ids, expert_ids, sorted_cap, blocks_cap);
+  if (e >= 0) {
+    const int q = seg[e] + wh[warp * E + e] + in_warp;
+    if (MOE_IN_BOUNDS(q >= 0 && q < sorted_cap)) sorted_ids[q] = static_cast<int32_t>(r);
+  }
 }
 
 size_t plan_ws_bytes(int64_t R, int E, int64_t* nchunks_out) {
@@ -320,6 +328,8 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
   w += round_up(R * 4, 256);
   ws.seg = reinterpret_cast<int32_t*>(w);
   ws.nchunks = static_cast<int>(R > 0 ? nchunks : 0);
+  ws.sorted_cap = sorted_cap;
+  ws.blocks_cap = blocks_cap;
 
   const size_t smem = static_cast<size_t>(kChunkWarps) * E * sizeof(int32_t);
   static bool attr_set[64] = {};
@@ -333,7 +343,8 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
   if (R <= kSmallRoutes && E <= kSmallMaxExperts) {
     const size_t small_smem = static_cast<size_t>(kScanThreads / 32) * E * sizeof(int32_t);
     MOE_CUDA_TRY(launch_pdl(plan_small_kernel, dim3(1), dim3(kScanThreads), small_smem, stream, 1, topk_ids, id_bits,
-                            R, E, block_m, sorted_token_ids, expert_ids, num_tokens_post_padded));
+                            R, E, block_m, sorted_token_ids, expert_ids, num_tokens_post_padded, sorted_cap,
+                            blocks_cap));
     return MOE_OK;
   }
   if (R > 0) {
@@ -352,3 +363,5 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

@@ -289,3 +289,5 @@ moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, i
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

@@ -145,3 +145,5 @@ moe_status moe_route_topk(const void* logits, int logit_dtype, int64_t M, int E,
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(32 * kUpWarps, 4) vec_up_kernel(const VecUpPar
   pdl_wait();
   // the down kernel reads the plan before its own wait: release it only now
   pdl_launch_dependents();
+  if (!MOE_IN_BOUNDS(b < p.nblocks)) return;
   // extent, expert and the block's route ids in one round trip (slots of
   // blocks inside the plan capacity are always readable)
   int ids[4];
@@ -210,7 +211,8 @@ __global__ void __launch_bounds__(32 * kUpWarps, 4) vec_up_kernel(const VecUpPar
       const int c = threadIdx.x;
       const float g = s_part[0][0][c] + s_part[1][0][c];
       const float u = s_part[0][1][c] + s_part[1][1][c];
-      p.h[static_cast<int64_t>(route) * p.I + c0 + c] = __fmul_rn(silu_f32(g), u);
+      if (MOE_IN_BOUNDS(route < p.R && c0 + c < p.I))
+        p.h[static_cast<int64_t>(route) * p.I + c0 + c] = __fmul_rn(silu_f32(g), u);
     }
     // s_act, s_as and s_part are rewritten for the next route
     __syncthreads();
@@ -346,6 +348,7 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
 
   const int64_t tok_lo = nh > 0 ? sm.held[0].route / p.top_k : 0;
   const int ntok = nh > 0 ? static_cast<int>(sm.held[nh - 1].route / p.top_k - tok_lo) + 1 : 0;
+  if (!MOE_IN_BOUNDS(ntok <= kVecMaxTokens)) return;  // (uniform over the CTA)
 
   for (int j0 = 0; j0 < nh; j0 += kJB) {
     if (j0 > 0) {
@@ -359,7 +362,9 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
 #pragma unroll
     for (int i = 0; i < kRq; ++i) {
       const int jj = warp + 4 * i;
-      const float* hrow = p.h + static_cast<int64_t>(jj < nb ? sm.held[j0 + jj].route : 0) * p.I;
+      int hr_route = jj < nb ? sm.held[j0 + jj].route : 0;
+      if (!MOE_IN_BOUNDS(hr_route >= 0 && hr_route < p.R)) hr_route = 0;
+      const float* hrow = p.h + static_cast<int64_t>(hr_route) * p.I;
 #pragma unroll
       for (int g = 0; g < kU; ++g)
         hv[i][g] = jj < nb ? __ldcg(reinterpret_cast<const float4*>(hrow + 128 * g) + lane)
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
           *reinterpret_cast<float4*>(&sm.u.b.q[jj][apos(128 * g + 4 * lane)]) =
               make_float4(qlo.x, qlo.y, qhi.x, qhi.y);
           if (lane == 0) sm.u.b.s[jj][g] = s;
-          if (p.dbg_q && blockIdx.x == 0) {
+          if (p.dbg_q && blockIdx.x == 0 && MOE_IN_BOUNDS(slot >= 0 && slot < p.nblocks * p.block_m)) {
             *reinterpret_cast<uint32_t*>(p.dbg_q + static_cast<int64_t>(slot) * p.I + 128 * g + 4 * lane) =
                 static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
             if (lane == 0) p.dbg_s[static_cast<int64_t>(slot) * kU + g] = s;
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
         y += __shfl_xor_sync(0xffffffffu, y, 2);
         y += __shfl_xor_sync(0xffffffffu, y, 4);
         const HeldRoute hr = sm.held[j0 + jj];
-        if (l8 == 0 && rowok) {
+        if (l8 == 0 && rowok && MOE_IN_BOUNDS(hr.route / p.top_k - tok_lo >= 0 && hr.route / p.top_k - tok_lo < ntok)) {
           float& a = sm.acc[hr.route / p.top_k - tok_lo][4 * warp + (lane >> 3)];
           a = __fadd_rn(a, __fmul_rn(y, hr.weight));
         }
@@ -440,7 +445,8 @@ __global__ void __launch_bounds__(128) vec_down_kernel(const VecDownParams p) {
   for (int i = threadIdx.x; i < ntok * kDnRows; i += nthreads) {
     const int tt = i / kDnRows, rr = i % kDnRows;
     const int orow = row0 + rr;
-    if (orow < p.H) p.out[(tok_lo + tt) * p.H + orow] = __bfloat16_as_ushort(__float2bfloat16_rn(sm.acc[tt][rr]));
+    if (orow < p.H && MOE_IN_BOUNDS(static_cast<int64_t>(tok_lo + tt) * p.top_k < p.R))
+      p.out[(tok_lo + tt) * p.H + orow] = __bfloat16_as_ushort(__float2bfloat16_rn(sm.acc[tt][rr]));
   }
 }
 
@@ -477,3 +483,5 @@ moe_status launch_vector_path(const VecUpParams& up, const VecDownParams& dn, cu
 }
 
 }  // namespace moe
+
+MOE_BOUNDS_TU()

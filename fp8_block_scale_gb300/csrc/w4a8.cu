@@ -202,6 +202,8 @@ struct W4Plan {
   const int32_t* expert_ids;
   const int32_t* ntpp;
   int R, top_k, block_m, E;
+  int64_t sorted_cap;  // entries of sorted_ids
+  int64_t nblocks;     // entries of expert_ids
 };
 
 // The plan block's expert (or -1 when the block holds no work) and its valid
@@ -210,6 +212,7 @@ __device__ __forceinline__ int block_rows(const W4Plan& pl, int b, int* s_rid, i
                                           bool report) {
   const int64_t P = *pl.ntpp;
   if (static_cast<int64_t>(b) * pl.block_m >= P) return -1;
+  if (!MOE_IN_BOUNDS(b < pl.nblocks)) return -1;
   const int e = pl.expert_ids[b];
   if (e < 0 || e >= pl.E) {
     if (report && e != -1 && threadIdx.x == 0 && status) atomicOr(status, MOE_DEV_BAD_EXPERT);
@@ -220,6 +223,7 @@ __device__ __forceinline__ int block_rows(const W4Plan& pl, int b, int* s_rid, i
     for (int r = 0; r < pl.block_m; ++r) {
       const int64_t slot = static_cast<int64_t>(b) * pl.block_m + r;
       if (slot >= P) break;
+      if (!MOE_IN_BOUNDS(slot < pl.sorted_cap && nv < kW4MaxBlockM)) break;
       const int id = pl.sorted_ids[slot];
       if (id >= 0 && id < pl.R) s_rid[nv++] = id;
     }
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(kW4Threads) w4a8_up_kernel(const W4UpParams p)
       for (int rr = 0; rr < kRowChunk; ++rr) {
         if (r0 + rr < nv) {
           const float g = warp_sum(ag[rr]), u = warp_sum(au[rr]);
-          if (lane == 0) {
+          if (lane == 0 && MOE_IN_BOUNDS(j < I)) {
             const float as = s_as[r0 + rr];
             const float gv = __fmul_rn(g, as), uv = __fmul_rn(u, as);
             p.h[static_cast<int64_t>(s_rid[r0 + rr]) * I + j] = __fmul_rn(silu_f32(gv), uv);
@@ -329,12 +333,14 @@ __global__ void __launch_bounds__(kW4Threads) w4a8_requant_kernel(const W4Requan
   const int b = blockIdx.x;
   const int64_t P = *p.pl.ntpp;
   if (static_cast<int64_t>(b) * p.pl.block_m >= P) return;
+  if (!MOE_IN_BOUNDS(b < p.pl.nblocks)) return;
   const int e = p.pl.expert_ids[b];
   if (e < 0 || e >= p.pl.E) return;
   const int I = p.I;
   for (int r = 0; r < p.pl.block_m; ++r) {
     const int64_t slot = static_cast<int64_t>(b) * p.pl.block_m + r;
     if (slot >= P) break;
+    if (!MOE_IN_BOUNDS(slot < p.pl.sorted_cap)) break;
     const int id = p.pl.sorted_ids[slot];
     if (id < 0 || id >= p.pl.R) continue;            // the same for every thread of the CTA
     const float* hr = p.h + static_cast<int64_t>(id) * I;
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kW4Threads) w4a8_down_kernel(const W4DownParam
       for (int rr = 0; rr < kRowChunk; ++rr) {
         if (r0 + rr < nv) {
           const float v = warp_sum(acc[rr]);
-          if (lane == 0) {
+          if (lane == 0 && MOE_IN_BOUNDS(hh < H)) {
             const float yv = __fmul_rn(v, s_s[r0 + rr]);
             p.y[static_cast<int64_t>(s_rid[r0 + rr]) * H + hh] = __fmul_rn(yv, s_w[r0 + rr]);
           }
@@ -551,7 +557,7 @@ moe_status moe_w4a8_forward(const moe_w4a8_args* a, moe_stream_t stream) {
   float* s = reinterpret_cast<float*>(ws + wl.s_off);
   float* y = reinterpret_cast<float*>(ws + wl.y_off);
   const W4Plan pl{a->sorted_token_ids, a->expert_ids, a->num_tokens_post_padded, static_cast<int>(R), a->top_k,
-                  a->block_m, a->E};
+                  a->block_m, a->E, a->sorted_cap, a->blocks_cap};
   const unsigned nblocks = static_cast<unsigned>(a->blocks_cap);
 
   MOE_CUDA_TRY(cudaMemsetAsync(rvalid, 0, static_cast<size_t>(R) * 4, stream));
@@ -564,6 +570,7 @@ moe_status moe_w4a8_forward(const moe_w4a8_args* a, moe_stream_t stream) {
     gp.num_post_padded = a->num_tokens_post_padded;
     gp.status = a->device_status;
     gp.nblocks = a->blocks_cap;
+    gp.sorted_cap = a->sorted_cap;
     gp.R = static_cast<int>(R);
     gp.top_k = a->top_k;
     gp.block_m = a->block_m;
@@ -618,3 +625,5 @@ moe_status moe_w4a8_forward(const moe_w4a8_args* a, moe_stream_t stream) {
 }
 
 }  // extern "C"
+
+MOE_BOUNDS_TU()

@@ -97,7 +97,7 @@ __device__ __forceinline__ bool w4_tile(const W4GemmParams& p, const W4Ctl* ctl,
     e = ctl->expert[b];
   } else {
     nb = 1;
-    e = p.expert_ids[b];
+    e = MOE_IN_BOUNDS(b < p.nblocks) ? p.expert_ids[b] : -1;
   }
   return nb > 0 && e >= 0 && e < p.E;
 }
@@ -176,10 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = 4 * lane + i;
+        const int64_t slot = static_cast<int64_t>(b) * p.block_m + r;
         int id = -1;
-        if (r < rows) id = p.sorted_ids[static_cast<int64_t>(b) * p.block_m + r];
+        if (r < rows && MOE_IN_BOUNDS(slot < p.sorted_cap)) id = p.sorted_ids[slot];
         const bool route = id >= 0 && id < p.R;
         ids[i] = route ? (p.up ? id / p.top_k : id) : 0;
+        if (!MOE_IN_BOUNDS(ids[i] < p.rows_total)) ids[i] = 0;
       }
       const uint32_t tx = kWTx + kSBytes + static_cast<uint32_t>(nmma) * kTK;
       const int wrow = p.up ? e * p.w_rows + wt * 64 : e * p.w_rows + wt * kTM;
@@ -195,21 +197,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, tx);
           const uint32_t w_dst = smem_u32(sW + s * kWBytes);
           const uint32_t s_dst = smem_u32(sS + s * kSBytes);
-          if (p.up) {
-            // 64 gate rows, then the 64 matching up rows (I rows further)
-            tma_load_2d(w_dst, &tmW, full, kb * kTK, wrow);
-            tma_load_2d(w_dst + 64 * kTK, &tmW, full, kb * kTK, wrow + p.I);
-            tma_load_2d(s_dst, &tmS, full, kb * 4, wrow);
-            tma_load_2d(s_dst + 64 * 16, &tmS, full, kb * 4, wrow + p.I);
-          } else {
-            tma_load_2d(w_dst, &tmW, full, kb * kTK, wrow);
-            tma_load_2d(s_dst, &tmS, full, kb * 4, wrow);
+          // 64 gate rows, then the 64 matching up rows (I rows further); or 128 W2 rows
+          for (int part = 0; part < (p.up ? 2 : 1); ++part) {
+            int wx = kb * kTK, wy = wrow + part * p.I, sx = kb * 4, sy = wy;
+            MOE_CHECK_BOX(wx, wy, static_cast<int64_t>(p.nkb) * kTK, static_cast<int64_t>(p.E) * p.w_rows, 32);
+            MOE_CHECK_BOX(sx, sy, static_cast<int64_t>(p.nkb) * 4, static_cast<int64_t>(p.E) * p.w_rows, 4);
+            tma_load_2d(w_dst + part * 64 * kTK, &tmW, full, wx, wy);
+            tma_load_2d(s_dst + part * 64 * 16, &tmS, full, sx, sy);
           }
         }
         __syncwarp();
+        int gx = kb * kTK;
+        if (!MOE_IN_BOUNDS(gx % 16 == 0 && gx < p.nkb * kTK)) gx = 0;
         if (mine)
-          tma_gather4_rows(smem_u32(sB + s * kBBytes) + 512u * lane, &tmB, full, kb * kTK, ids[0], ids[1], ids[2],
-                           ids[3]);
+          tma_gather4_rows(smem_u32(sB + s * kBBytes) + 512u * lane, &tmB, full, gx, ids[0], ids[1], ids[2], ids[3]);
         ++it;
       }
     }
@@ -279,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 2) {
         for (int c = lane; c < kMaxN; c += 32) {
           int id = -1;
-          if (c < rows) id = p.sorted_ids[static_cast<int64_t>(b) * p.block_m + c];
+          const int64_t slot = static_cast<int64_t>(b) * p.block_m + c;
+          if (c < rows && MOE_IN_BOUNDS(slot < p.sorted_cap)) id = p.sorted_ids[slot];
           const bool route = id >= 0 && id < p.R;
           ctl->route[c] = route ? id : -1;
           ctl->cs[c] = route ? (p.up ? p.a_scale[id / p.top_k] : p.s_inter[id]) : 0.f;
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kMaxN / 2; ++c) {
             if (c < ncols) {
               const int rt = ctl->route[c0 + c];
-              if (rt >= 0) {
+              if (rt >= 0 && MOE_IN_BOUNDS(rt < p.R && j < p.I)) {
                 const float g = __fmul_rn(acc[c], ctl->cs[c0 + c]);
                 p.h[static_cast<int64_t>(rt) * p.I + j] = __fmul_rn(silu_f32(g), ctl->xchg[row][c0 + c]);
               }
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kMaxN / 2; ++c) {
           if (c < ncols) {
             const int rt = ctl->route[c0 + c];
-            if (rt >= 0)
+            if (rt >= 0 && MOE_IN_BOUNDS(rt < p.R && hcol < p.H))
               p.y[static_cast<int64_t>(rt) * p.H + hcol] =
                   __fmul_rn(__fmul_rn(acc[c], ctl->cs[c0 + c]), ctl->cw[c0 + c]);
           }
@@ -402,6 +404,7 @@ moe_status launch_w4a8_tc_gemm(const W4GemmTensors& t, W4GemmParams p, int sms, 
       encode_tensor_map_2d(&mb, t.rows, t.k, t.rows_total, t.k, kTK, 1, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
   p.group = p.block_m >= kMaxN ? 1 : kMaxN / p.block_m;
+  p.rows_total = static_cast<int64_t>(t.rows_total);
   p.nkb = static_cast<int>(t.k / kTK);
   const int64_t tiles = p.nblocks * p.ntw;
   if (tiles <= 0) return MOE_OK;
@@ -412,3 +415,5 @@ moe_status launch_w4a8_tc_gemm(const W4GemmTensors& t, W4GemmParams p, int sms, 
 }
 
 }  // namespace moe
+
+MOE_BOUNDS_TU()

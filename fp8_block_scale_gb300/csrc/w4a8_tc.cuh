@@ -17,6 +17,8 @@ struct W4GemmParams {
   float* y;                        // down out: [R, H] y * s * w by route id
   int32_t* status;                 // nullable
   int64_t nblocks;                 // plan blocks the grid walks
+  int64_t sorted_cap;              // entries of sorted_ids
+  int64_t rows_total;              // rows of the gathered tensor (set by the launcher)
   int R, top_k, block_m, E, H, I;
   int up;                          // 1: gate/up projection, 0: down projection
   int ntw;                         // weight tiles per plan block: I / 64 (gate/up) or H / 128 (down)

@@ -347,6 +347,35 @@ moe_status moe_selftest_wait_timeout(uint32_t limit_us, int32_t* device_status, 
                                      moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Bounds-checking build.  A library compiled with -DMOE_DEBUG_BOUNDS
+ * (libmoe_fp8_debug.so from the package's build script) checks, before each
+ * access, every global index its kernels derive from data or tiling (plan
+ * entries, route, token, slot and expert ids, workspace offsets) and every
+ * tensor-copy coordinate (in range, and the innermost one 16-byte aligned).
+ * A failed check is counted in a device-side record, the access is skipped
+ * (a tensor copy is moved to coordinate 0 so its barrier still completes)
+ * and the kernel carries on; nothing traps.  Results are then unspecified,
+ * but the context stays usable.  The normal build compiles the checks away.
+ * ------------------------------------------------------------------------ */
+/* 1 in the bounds-checking build, 0 otherwise. */
+int moe_debug_bounds_enabled(void);
+/* Waits for the device (cudaDeviceSynchronize), then writes to *failures the
+ * number of failed checks since the library loaded or the last reset, and
+ * to *first_file / *first_line (both nullable) the source file (a static
+ * string, NULL when there was none) and line of the first failure in the
+ * first file that has one.  reset != 0 zeroes the records afterwards.  In the
+ * normal build *failures = 0.  MOE_ERR_NULL if failures is NULL, MOE_ERR_CUDA
+ * if the synchronisation or a read fails. */
+moe_status moe_debug_bounds_read(uint64_t* failures, const char** first_file, int32_t* first_line, int reset);
+/* Self-test of the checks: one thread reads data[probe] into *out.  In the
+ * bounds-checking build a probe outside [0, n) fails the kernel's check,
+ * which counts it and writes -1 instead of reading; in the normal build such
+ * a probe is refused on the host (MOE_ERR_SHAPE) and nothing is launched.
+ *  data  [n] int32, device memory;  out  [1] int32, device memory (written)
+ * n >= 1, else MOE_ERR_SHAPE; asynchronous on `stream`. */
+moe_status moe_debug_bounds_selftest(const int32_t* data, int n, int probe, int32_t* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free forward.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot call cudaMalloc: engines that
  * hand all of device memory to their own pool at start-up and forbid any

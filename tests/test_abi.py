@@ -227,3 +227,32 @@ def test_selftest_host_validation_without_gpu(lib):
     assert f(1000, _fake(256), None, None) == 1
     assert f(0, _fake(256), _fake(512), None) == 2               # limit below 1 us
     assert f(1000001, _fake(256), _fake(512), None) == 2         # limit above 1 s
+
+
+@pytest.fixture(scope="module")
+def debug_lib():
+    from fp8_block_scale_gb300 import _lib
+    from fp8_block_scale_gb300.build import build
+    build(debug_bounds=True)
+    return _lib.load(_lib.LIB_DEBUG_PATH)
+
+
+def test_debug_bounds_switch_without_gpu(lib, debug_lib):
+    """The normal build has no bounds records (reading them needs no device);
+    the bounds-checking build says so and exports the same entry points."""
+    n = ctypes.c_uint64(7)
+    f = ctypes.c_char_p(b"x")
+    line = ctypes.c_int32(3)
+    assert lib.moe_debug_bounds_enabled() == 0
+    assert lib.moe_debug_bounds_read(ctypes.byref(n), ctypes.byref(f), ctypes.byref(line), 1) == 0
+    assert (n.value, f.value, line.value) == (0, None, 0)
+    assert lib.moe_debug_bounds_read(None, None, None, 0) == 1
+    # an out-of-range probe is refused on the host by the normal build
+    p = _fake(4096)
+    assert lib.moe_debug_bounds_selftest(p, 4, 4, p, None) == 2
+    assert lib.moe_debug_bounds_selftest(p, 4, -1, p, None) == 2
+    assert lib.moe_debug_bounds_selftest(None, 4, 0, p, None) == 1
+    assert lib.moe_debug_bounds_selftest(p, 0, 0, p, None) == 2
+    assert debug_lib.moe_debug_bounds_enabled() == 1
+    missing = [name for name in _declared_functions() if not hasattr(debug_lib, name)]
+    assert not missing, missing
