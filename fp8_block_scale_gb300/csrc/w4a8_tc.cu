@@ -22,7 +22,9 @@
 //               slice, each into its own N columns of one of two TMEM buffers;
 //   warps 2..9  epilogue: warp w owns TMEM lane quarter w % 4 (32 weight
 //               rows) and half of the route columns; per slice it adds each
-//               K32 partial times its row's scale to FP32 registers.
+//               K32 partial times its row's scale to FP32 registers;
+//   warp 10     route tables, one tile ahead: each column's route id and its
+//               scales, in two shared-memory tables.
 // Gate/up tile = 64 gate rows + the 64 matching up rows of the logical W13:
 // at the tile end the up rows' values pass through shared memory to the gate
 // rows' threads, which write silu(g) * u by route id.  Down tile = 128 W2
@@ -38,7 +40,8 @@ constexpr int kTK = 128;                  // K elements per stage
 constexpr int kMaxN = 64;                 // route rows per tile (MMA N <= 64)
 constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kLoaderWarp = 2 + kEpiWarps;  // after the producer, the MMA warp and the epilogue
+constexpr int kThreads = 32 * (kLoaderWarp + 1);
 constexpr int kWBytes = kTM * kTK;        // 16 KiB in shared memory (padded E2M1)
 constexpr int kWTx = kTM * kTK / 2;       // the packed bytes the copy engine counts
 constexpr int kBBytes = kMaxN * kTK;      // 8 KiB of activation / intermediate rows
@@ -51,12 +54,15 @@ struct alignas(16) W4Ctl {
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t rfull[2];                      // a tile's route table is written (producer)
+  uint64_t rempty[2];                     // ... and has been used (every epilogue warp)
   uint32_t tmem_base;
   int abort_flag;
   int pad[2];
-  int32_t route[kMaxN];                   // the tile's route id per column (-1 = none)
-  float cs[kMaxN];                        // per column: activation scale (up) / intermediate scale (down)
-  float cw[kMaxN];                        // down: route weight x routed scale
+  // route tables of two consecutive tiles, filled by the producer
+  int32_t route[2][kMaxN];                // the tile's route id per column (-1 = none)
+  float cs[2][kMaxN];                     // per column: activation scale (up) / intermediate scale (down)
+  float cw[2][kMaxN];                     // down: route weight x routed scale
   float xchg[64][kMaxN + 1];              // up: up-row values handed to the gate rows' threads
   int32_t expert[kMaxBlocks];
   uint8_t lead[kMaxBlocks];               // blocks in the group this block leads (0: not a group leader)
@@ -123,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->tfull[i]), 1);
       mbar_init(smem_u32(&ctl->tempty[i]), kEpiWarps);
+      mbar_init(smem_u32(&ctl->rfull[i]), 1);
+      mbar_init(smem_u32(&ctl->rempty[i]), kEpiWarps);
     }
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -255,13 +263,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0) drain_wait(smem_u32(&ctl->tfull[(it - 1) & 1u]), ((it - 1) >> 1) & 1u);
     }
     __syncwarp();
+  } else if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------ route tables
+    // One tile ahead of the epilogue: the tile's route id per column and the
+    // column scales (two dependent global loads), so that the epilogue starts
+    // a tile without a round trip to global memory.
+    uint32_t tc = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int b, wt, e, nb;
+      if (!w4_tile(p, ctl, tile, nvalid, b, wt, e, nb)) continue;
+      const int rows = nb * p.block_m;
+      const int par = tc & 1;
+      if (!warp_wait(smem_u32(&ctl->rempty[par]), ((tc >> 1) & 1u) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int c = lane; c < kMaxN; c += 32) {
+        int id = -1;
+        const int64_t slot = static_cast<int64_t>(b) * p.block_m + c;
+        if (c < rows && MOE_IN_BOUNDS(slot < p.sorted_cap)) id = p.sorted_ids[slot];
+        const bool route = id >= 0 && id < p.R;
+        ctl->route[par][c] = route ? id : -1;
+        ctl->cs[par][c] = route ? (p.up ? p.a_scale[id / p.top_k] : p.s_inter[id]) : 0.f;
+        ctl->cw[par][c] = (route && !p.up) ? __fmul_rn(p.topk_w[id], p.routed_scale) : 0.f;
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->rfull[par]));
+      ++tc;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;  // weight row of the tile
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t it = 0;
+    uint32_t it = 0, tc = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int b, wt, e, nb;
@@ -276,19 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nmma = (rows + 15) & ~15;
       const int ncols = nmma / 2;           // this thread's route columns: half * ncols ..
       const int c0 = half * ncols;
-      // the tile's routes and their column scales (read once per tile)
-      if (warp == 2) {
-        for (int c = lane; c < kMaxN; c += 32) {
-          int id = -1;
-          const int64_t slot = static_cast<int64_t>(b) * p.block_m + c;
-          if (c < rows && MOE_IN_BOUNDS(slot < p.sorted_cap)) id = p.sorted_ids[slot];
-          const bool route = id >= 0 && id < p.R;
-          ctl->route[c] = route ? id : -1;
-          ctl->cs[c] = route ? (p.up ? p.a_scale[id / p.top_k] : p.s_inter[id]) : 0.f;
-          ctl->cw[c] = (route && !p.up) ? __fmul_rn(p.topk_w[id], p.routed_scale) : 0.f;
-        }
-      }
-      named_barrier(1, 32 * kEpiWarps);
+      // the tile's routes and their column scales (the producer's table)
+      const int par = tc & 1;
+      if (ok) ok = warp_wait(smem_u32(&ctl->rfull[par]), (tc >> 1) & 1u, abort_flag);
+      const int32_t* t_route = ctl->route[par];
+      const float* t_cs = ctl->cs[par];
+      const float* t_cw = ctl->cw[par];
 
       float acc[kMaxN / 2];
 #pragma unroll
@@ -332,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row >= 64) {
 #pragma unroll
           for (int c = 0; c < kMaxN / 2; ++c)
-            if (c < ncols) ctl->xchg[row - 64][c0 + c] = __fmul_rn(acc[c], ctl->cs[c0 + c]);
+            if (c < ncols) ctl->xchg[row - 64][c0 + c] = __fmul_rn(acc[c], t_cs[c0 + c]);
         }
         named_barrier(1, 32 * kEpiWarps);
         if (row < 64 && ok) {
@@ -340,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kMaxN / 2; ++c) {
             if (c < ncols) {
-              const int rt = ctl->route[c0 + c];
+              const int rt = t_route[c0 + c];
               if (rt >= 0 && MOE_IN_BOUNDS(rt < p.R && j < p.I)) {
-                const float g = __fmul_rn(acc[c], ctl->cs[c0 + c]);
+                const float g = __fmul_rn(acc[c], t_cs[c0 + c]);
                 p.h[static_cast<int64_t>(rt) * p.I + j] = __fmul_rn(silu_f32(g), ctl->xchg[row][c0 + c]);
               }
             }
@@ -353,15 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kMaxN / 2; ++c) {
           if (c < ncols) {
-            const int rt = ctl->route[c0 + c];
+            const int rt = t_route[c0 + c];
             if (rt >= 0 && MOE_IN_BOUNDS(rt < p.R && hcol < p.H))
               p.y[static_cast<int64_t>(rt) * p.H + hcol] =
-                  __fmul_rn(__fmul_rn(acc[c], ctl->cs[c0 + c]), ctl->cw[c0 + c]);
+                  __fmul_rn(__fmul_rn(acc[c], t_cs[c0 + c]), t_cw[c0 + c]);
           }
         }
       }
-      // the tile's route table and exchange rows are rewritten by the next tile
+      // the exchange rows are rewritten by the next tile; the route table
+      // goes back to the producer
       named_barrier(1, 32 * kEpiWarps);
+      if (ok && lane == 0) mbar_arrive(smem_u32(&ctl->rempty[par]));
+      ++tc;
     }
   }
 
