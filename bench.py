@@ -659,6 +659,24 @@ def extra_sweep(cfg, prob, flush, peaks):
                      "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"],
                                     "combine": r["combine_ms"]}}
         del p
+    # the headline shape with power-of-two block scales on both operands,
+    # once with the FP32 promotion and once with the block-scaled MMA
+    # (MOE_SCALES_UE8M0) on the same inputs
+    from fp8_block_scale_gb300 import _lib as L
+    c = W.CONFIGS["prefill_8192"].with_(name="prefill_8192_ue8m0", ue8m0=True, act_ue8m0=True)
+    p = DeviceProblem(c)
+    w = work(c, p.routing.topk_ids.to(torch.int64).numpy())
+    t_roof = max(w["total"]["flop"] / (fp8_peak * 1e12), w["total"]["bytes"] / (hbm * 1e9))
+    for label, mode in (("fp32_promotion", L.SCALES_FP32), ("block_scaled_mma", L.SCALES_UE8M0)):
+        p.scale_mode = mode
+        r = measure(p, 10, 3, flush)
+        out[f"prefill_8192_ue8m0_{label}"] = {
+            "ms_step": r["step_ms"], "ms_forward": r["forward_ms"],
+            "tflops_step": w["total"]["flop"] / (r["step_ms"] * 1e-3) / 1e12,
+            "frac_roofline_step": t_roof / (r["step_ms"] * 1e-3),
+            "ms_kernels": {"stage": r["stage_ms"], "up": r["up_ms"], "down": r["down_ms"], "combine": r["combine_ms"]}}
+    del p
+    torch.cuda.empty_cache()
     # the other two workloads at their own sizes and weights
     for name in ("skewed", "large"):
         c = W.CONFIGS[name]
@@ -781,6 +799,10 @@ def main():
     ap.add_argument("--oracle-child", nargs=3, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--w4a8", action="store_true",
                     help="time only the E2M1-K32 weight path at 1 and 1024 tokens (one JSON line)")
+    ap.add_argument("--w4a8-tokens", default="1,1024", help="with --w4a8: token counts, comma-separated")
+    ap.add_argument("--w4a8-paths", default="tc,cuda_cores", help="with --w4a8: tc and/or cuda_cores")
+    ap.add_argument("--w4a8-steps", type=int, default=5, help="with --w4a8: timed forwards per configuration")
+    ap.add_argument("--w4a8-warmup", type=int, default=3, help="with --w4a8: untimed forwards first")
     args = ap.parse_args()
     if args.oracle_child:
         _oracle_child(*args.oracle_child)
@@ -791,8 +813,15 @@ def main():
         L.load()
         peaks = load_peaks()
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        res = {f"w4a8_e288_m{M}": measure_w4a8(M, flush, peaks) for M in (1, 1024)}
-        res.update({f"w4a8_e288_m{M}_cuda_cores": measure_w4a8(M, flush, peaks, path=1) for M in (1, 1024)})
+        tokens = [int(t) for t in args.w4a8_tokens.split(",")]
+        paths = args.w4a8_paths.split(",")
+        res = {}
+        for path, suffix in ((0, ""), (1, "_cuda_cores")):
+            if ("tc" if path == 0 else "cuda_cores") not in paths:
+                continue
+            for M in tokens:
+                res[f"w4a8_e288_m{M}{suffix}"] = measure_w4a8(M, flush, peaks, steps=args.w4a8_steps,
+                                                               warmup=args.w4a8_warmup, path=path)
         print(json.dumps(res), flush=True)
         return
     if args.warmup < 3:

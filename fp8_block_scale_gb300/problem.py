@@ -101,7 +101,13 @@ class DeviceProblem:
         L.moe_plan(self.topk_ids, self.cfg.E, self.cfg.block_m, self.sorted_ids, self.expert_ids, self.ntpp,
                    self.plan_ws, stream)
 
-    def fwd_args(self, debug_q=None, debug_s=None, out=None, tile_mode=L.TILE_AUTO, scale_mode=L.SCALES_FP32):
+    # how the forward applies the block scales unless a call says otherwise
+    # (MOE_SCALES_UE8M0 needs power-of-two scales on both operands)
+    scale_mode = L.SCALES_FP32
+
+    def fwd_args(self, debug_q=None, debug_s=None, out=None, tile_mode=L.TILE_AUTO, scale_mode=None):
+        if scale_mode is None:
+            scale_mode = self.scale_mode
         args = L.make_fwd_args(self.a, self.a_scale, self.w13, self.w13_scale, self.w2, self.w2_scale,
                                self.topk_weights, self.sorted_ids, self.expert_ids, self.ntpp,
                                self.out if out is None else out, self.workspace, self.cfg.top_k, self.cfg.block_m,
