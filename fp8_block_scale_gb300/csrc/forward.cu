@@ -88,12 +88,15 @@ struct SmemCtl {
   int abort_flag;
   int last_flag;                   // split-K: this CTA completed the tile's sum
   int pad;
-  union alignas(16) Scratch {
+  union alignas(128) Scratch {  // (tensor stores read 128-byte aligned shared memory)
     struct {
       float xchg[2][2][kTileM];                 // [tile parity][column half][row] amax exchange
       // block-scaled mode: per stage, the slice's UE8M0 scale-factor rows
       // for the tensor-memory copy (A: 32 rows x 16 bytes, then B)
       alignas(16) uint8_t sf[kMaxStages][1024];
+      // per epilogue warp, the codes of its 32 rows x 32 columns on their way
+      // to q_inter through tensor stores
+      alignas(128) uint8_t qst[kNumEpiWarps][32 * 32];
     } up;
     uint32_t yt[kNumEpiWarps][32][20];          // down: per-warp transpose of 32 rows x 32 BF16 (padded rows)
   } u;
@@ -105,10 +108,13 @@ struct SmemCtl {
 static_assert(offsetof(SmemCtl, u) % 16 == 0, "scratch alignment");
 static_assert(sizeof(SmemCtl) % 16 == 0, "control block size");
 
+static_assert(alignof(SmemCtl) == 128 && offsetof(SmemCtl, u) % 128 == 0, "control block alignment");
+
+// 1024 bytes for aligning the operand stages, 128 for aligning the control block.
 template <bool kPair>
 constexpr size_t smem_bytes() {
   return 1024 + static_cast<size_t>(Cfg<kPair>::kStages) * (kABytes + Cfg<kPair>::kBStage + sizeof(StageExtra)) +
-         sizeof(SmemCtl);
+         128 + sizeof(SmemCtl);
 }
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 
@@ -166,6 +172,7 @@ struct GemmParams {
   uint32_t* gen;               // up: forward stamp, advanced once per forward
   int64_t a_rows;              // rows of the A operand's tensor (M tokens, or sorted_cap plan slots)
   int64_t q_rows;              // up: rows of q_inter (sorted_cap)
+  int qbox;                    // up: rows per tensor store of codes (8, 16 or 32; divides block_m)
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -300,7 +307,7 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 template <bool kUp, bool kPair, bool kBS = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmQ, const GemmParams p) {
   static_assert(!kBS || (kUp && !kPair), "block-scaled mode: gate/up on single CTAs");
   using C = Cfg<kPair>;
   constexpr int kStages = C::kStages;
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   StageExtra* sX = reinterpret_cast<StageExtra*>(sB + kStages * kBStage);
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sX + kStages);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>((reinterpret_cast<uintptr_t>(sX + kStages) + 127) & ~uintptr_t(127));
   volatile int* abort_flag = &ctl->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -815,20 +822,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // h / s as h * (1/s): the two roundings can move a value across an
         // E4M3 rounding midpoint only when it lies within an ulp of it
         const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+        uint32_t packed[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const uint16_t lo = cvt_e4m3x2(__fmul_rn(acc[4 * w + 0], inv), __fmul_rn(acc[4 * w + 1], inv));
+          const uint16_t hi = cvt_e4m3x2(__fmul_rn(acc[4 * w + 2], inv), __fmul_rn(acc[4 * w + 3], inv));
+          packed[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        // The codes leave through tensor stores of whole row boxes: the warp's
+        // 32 rows are consecutive plan slots; boxes stop at the plan block's
+        // last row (the next block's slots belong to another CTA).
+        {
+          const int64_t wslot = MOE_SLOT - lane;  // the warp's first row
+          int nvr = MOE_HAS_ROWS ? p.block_m - 32 * (warp & 3) : 0;
+          nvr = nvr < 0 ? 0 : (nvr > 32 ? 32 : nvr);
+          if (!ok) nvr = 0;
+          uint8_t* stage = ctl->u.up.qst[warp - 2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (nvr > 0) {
+              if (r > 0) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
+              *reinterpret_cast<uint4*>(stage + 32 * lane) =
+                  make_uint4(packed[8 * r], packed[8 * r + 1], packed[8 * r + 2], packed[8 * r + 3]);
+              *reinterpret_cast<uint4*>(stage + 32 * lane + 16) =
+                  make_uint4(packed[8 * r + 4], packed[8 * r + 5], packed[8 * r + 6], packed[8 * r + 7]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                for (int r0 = 0; r0 < nvr; r0 += p.qbox) {
+                  int qx = 128 * t + 64 * half + 32 * r, qy = static_cast<int>(wslot) + r0;
+                  MOE_CHECK_BOX(qx, qy, p.I, p.q_rows - p.qbox + 1, 16);
+                  tma_store_2d(&tmQ, smem_u32(stage + 32 * r0), qx, qy);
+                }
+                bulk_commit();
+              }
+            }
+          }
+          if (nvr > 0 && lane == 0) bulk_wait_read_all();  // the stage is rewritten by the next tile
+          __syncwarp();
+        }
         if (ok && MOE_RVALID && MOE_IN_BOUNDS(MOE_SLOT < p.q_rows && MOE_SLOT < p.cap_pad)) {
           const int64_t slot = MOE_SLOT;
-          uint32_t packed[16];
-#pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const uint16_t lo = cvt_e4m3x2(__fmul_rn(acc[4 * w + 0], inv), __fmul_rn(acc[4 * w + 1], inv));
-            const uint16_t hi = cvt_e4m3x2(__fmul_rn(acc[4 * w + 2], inv), __fmul_rn(acc[4 * w + 3], inv));
-            packed[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-          }
           const int64_t qoff = slot * p.I + 128 * t + 64 * half;
-          uint4* qdst = reinterpret_cast<uint4*>(p.q_inter + qoff);
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            qdst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
           if (half == 0) p.s_inter_t[static_cast<int64_t>(t) * p.cap_pad + slot] = s;
           if (p.dbg_q) {
             uint4* ddst = reinterpret_cast<uint4*>(p.dbg_q + qoff);
@@ -876,6 +914,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       ++tcount;
     }
+    // the codes' tensor stores are complete before the grid is (the down
+    // kernel reads them after its dependency wait)
+    if (kUp && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1385,6 +1426,13 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       encode_tensor_map_2d(&tm_w2, a->w2, a->I, static_cast<uint64_t>(a->E) * a->H, a->I, 128, wbox,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
+  // tensor stores of the intermediate codes: boxes of 32 codes x qbox rows,
+  // qbox the largest of 32, 16, 8 that divides block_m
+  const int qbox = a->block_m % 32 == 0 ? 32 : (a->block_m % 16 == 0 ? 16 : 8);
+  CUtensorMap tm_qs;
+  if (encode_tensor_map_2d(&tm_qs, q_inter, a->I, a->sorted_cap, a->I, 32, static_cast<uint32_t>(qbox),
+                           CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return MOE_ERR_CUDA;
 
   if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[0], stream));
   if (nblocks > 0) {
@@ -1437,6 +1485,7 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
     p.H = a->H;
     p.q_rows = a->sorted_cap;
     p.a_rows = a->sorted_cap;
+    p.qbox = qbox;
 
     GemmParams up = p;
     up.a_scale_t = as_t;
@@ -1474,15 +1523,15 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       int64_t clusters = ceil_div(up_tiles, 2);
       if (clusters > pair_clusters) clusters = pair_clusters;
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, true>, dim3(static_cast<unsigned>(2 * clusters)),
-                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_a, tm_w13, up));
+                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_a, tm_w13, tm_qs, up));
     } else if (block_scaled) {
       const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false, true>, dim3(up_grid), dim3(kNumThreads),
-                              smem_bytes<false>(), stream, 1, tm_a, tm_w13, up));
+                              smem_bytes<false>(), stream, 1, tm_a, tm_w13, tm_qs, up));
     } else {
       const int up_grid = static_cast<int>(up_tiles < dev.sms ? up_tiles : dev.sms);
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<true, false>, dim3(up_grid), dim3(kNumThreads), smem_bytes<false>(),
-                              stream, 1, tm_a, tm_w13, up));
+                              stream, 1, tm_a, tm_w13, tm_qs, up));
     }
     if (ev) MOE_CUDA_TRY(cudaEventRecord(ev[2], stream));
 
@@ -1514,11 +1563,11 @@ moe_status moe_fp8_block_scale_forward(const moe_fwd_args* a, moe_stream_t strea
       int64_t clusters = ceil_div(dn_tiles, 2);
       if (clusters > pair_clusters) clusters = pair_clusters;
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<false, true>, dim3(static_cast<unsigned>(2 * clusters)),
-                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_q, tm_w2, dn));
+                              dim3(kNumThreads), smem_bytes<true>(), stream, 2, tm_q, tm_w2, tm_qs, dn));
     } else {
       const int dn_grid = static_cast<int>(dn_tiles < dev.sms ? dn_tiles : dev.sms);
       MOE_CUDA_TRY(launch_pdl(moe_gemm_kernel<false, false>, dim3(dn_grid), dim3(kNumThreads), smem_bytes<false>(),
-                              stream, 1, tm_q, tm_w2, dn));
+                              stream, 1, tm_q, tm_w2, tm_qs, dn));
     }
   } else if (ev) {
     MOE_CUDA_TRY(cudaEventRecord(ev[1], stream));
