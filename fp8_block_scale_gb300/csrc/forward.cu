@@ -991,11 +991,6 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
       if (route) p.rvalid[id] = *p.gen + 1u;
     }
     if (!route) continue;
-    for (int k = lane; k < nkb; k += 32) {
-      const float v = __ldg(p.a_scale + tok * nkb + k);
-      p.as_t[k * p.cap_pad + slot] = v;
-      if (p.check_pow2 && !ue8m0_ok(v)) report(p.status, MOE_DEV_BAD_SCALE);
-    }
     if (p.a_sorted && MOE_IN_BOUNDS(slot < p.a_rows)) {
       // up to 4 KB of the row in flight per warp (8 loads per lane) before the stores
       const uint4* src = reinterpret_cast<const uint4*>(p.a + tok * p.H);
@@ -1012,6 +1007,23 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
           const int c = c0 + 32 * j + lane;
           if (c < chunks) dst[c] = v[j];
         }
+      }
+    }
+  }
+  // activation scales transposed to [K slice][slot]: a warp per 32
+  // consecutive slots, lane = slot, so each slice's 32 scales are one
+  // 128-byte store (each lane walks its own token's scale row)
+  for (int64_t s0 = gtid / 32 * 32; s0 < nslots; s0 += nwarps * 32) {
+    const int64_t slot = s0 + lane;
+    int id = -1;
+    if (slot < nslots) id = p.sorted_ids[slot];
+    const bool route = id >= 0 && id < p.R;
+    const float* row = p.a_scale + (route ? static_cast<int64_t>(id / p.top_k) * nkb : 0);
+    if (slot < nslots && MOE_IN_BOUNDS(slot < p.cap_pad)) {
+      for (int k = 0; k < nkb; ++k) {
+        const float v = route ? __ldg(row + k) : 0.f;
+        p.as_t[k * p.cap_pad + slot] = v;
+        if (route && p.check_pow2 && !ue8m0_ok(v)) report(p.status, MOE_DEV_BAD_SCALE);
       }
     }
   }
