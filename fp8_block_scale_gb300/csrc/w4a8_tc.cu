@@ -201,17 +201,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t full = smem_u32(&ctl->full[s]);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, tx);
-          const uint32_t w_dst = smem_u32(sW + s * kWBytes);
-          const uint32_t s_dst = smem_u32(sS + s * kSBytes);
-          // 64 gate rows, then the 64 matching up rows (I rows further); or 128 W2 rows
-          for (int part = 0; part < (p.up ? 2 : 1); ++part) {
+        if (lane == 0) mbar_arrive_expect_tx(full, tx);
+        __syncwarp();
+        {
+          // one copy per lane (a thread's copies are issued one after
+          // another): lanes 0/1 the weight boxes of the 64 gate and 64 up
+          // rows (I rows further), or lane 0 the 128 W2 rows; lanes 2/3 the
+          // matching scale boxes
+          const int part = lane & 1;
+          if (lane < 4 && part < (p.up ? 2 : 1)) {
             int wx = kb * kTK, wy = wrow + part * p.I, sx = kb * 4, sy = wy;
-            MOE_CHECK_BOX(wx, wy, static_cast<int64_t>(p.nkb) * kTK, static_cast<int64_t>(p.E) * p.w_rows, 32);
-            MOE_CHECK_BOX(sx, sy, static_cast<int64_t>(p.nkb) * 4, static_cast<int64_t>(p.E) * p.w_rows, 4);
-            tma_load_2d(w_dst + part * 64 * kTK, &tmW, full, wx, wy);
-            tma_load_2d(s_dst + part * 64 * 16, &tmS, full, sx, sy);
+            if (lane < 2) {
+              MOE_CHECK_BOX(wx, wy, static_cast<int64_t>(p.nkb) * kTK, static_cast<int64_t>(p.E) * p.w_rows, 32);
+              tma_load_2d(smem_u32(sW + s * kWBytes) + part * 64 * kTK, &tmW, full, wx, wy);
+            } else {
+              MOE_CHECK_BOX(sx, sy, static_cast<int64_t>(p.nkb) * 4, static_cast<int64_t>(p.E) * p.w_rows, 4);
+              tma_load_2d(smem_u32(sS + s * kSBytes) + part * 64 * 16, &tmS, full, sx, sy);
+            }
           }
         }
         __syncwarp();
