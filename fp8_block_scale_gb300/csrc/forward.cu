@@ -15,7 +15,7 @@
 //      epilogue warps promote each slice in FP32 with the activation and
 //      weight block scales, then apply SwiGLU and requantise the 128
 //      intermediate columns of the tile to E4M3 (scale amax/448) into the
-//      workspace.
+//      workspace (the codes leave through tensor stores of row boxes).
 //   2. down (gemm kernel, kUp = false): intermediate rows x W2 tile, promoted
 //      with the intermediate and W2 block scales, times the route weight and
 //      routed scale, rounded to BF16 and stored as the route's row of the
