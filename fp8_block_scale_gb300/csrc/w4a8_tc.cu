@@ -37,23 +37,34 @@ namespace {
 
 constexpr int kTM = 128;                  // weight rows per tile (MMA M)
 constexpr int kTK = 128;                  // K elements per stage
-constexpr int kMaxN = 64;                 // route rows per tile (MMA N <= 64)
-constexpr int kStages = 6;
+// The kernel comes in two widths: up to 64 route rows per tile with two TMEM
+// buffers (each buffer: a slice's four K32 partials x 64 columns) and 6
+// stages, and, for small plans, up to 16 rows with eight buffers and 8
+// stages, so that the MMAs run up to eight slices ahead of the epilogue
+// instead of two.
+template <int kN>
+struct W4Cfg {
+  static constexpr int kMaxN = kN;                       // route rows per tile (MMA N)
+  static constexpr int kTBufs = 512 / (4 * kN);          // TMEM buffers: 2 or 8
+  static constexpr int kStages = kN == 64 ? 6 : 8;
+  static constexpr int kBBytes = kN * 128;               // activation / intermediate rows per stage
+};
 constexpr int kEpiWarps = 8;
 constexpr int kLoaderWarp = 2 + kEpiWarps;  // after the producer, the MMA warp and the epilogue
 constexpr int kThreads = 32 * (kLoaderWarp + 1);
 constexpr int kWBytes = kTM * kTK;        // 16 KiB in shared memory (padded E2M1)
 constexpr int kWTx = kTM * kTK / 2;       // the packed bytes the copy engine counts
-constexpr int kBBytes = kMaxN * kTK;      // 8 KiB of activation / intermediate rows
 constexpr int kSBytes = kTM * 16;         // four FP32 K32 scales per weight row
 constexpr int kMaxBlocks = 1024;          // plan blocks whose expert is cached in shared memory
-constexpr uint32_t kTmemCols = 512;       // 2 buffers x 4 K32 partials x kMaxN columns
+constexpr uint32_t kTmemCols = 512;       // kTBufs buffers x 4 K32 partials x kMaxN columns
 
+template <int kN>
 struct alignas(16) W4Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  static constexpr int kMaxN = kN;
+  uint64_t full[W4Cfg<kN>::kStages];
+  uint64_t empty[W4Cfg<kN>::kStages];
+  uint64_t tfull[W4Cfg<kN>::kTBufs];
+  uint64_t tempty[W4Cfg<kN>::kTBufs];
   uint64_t rfull[2];                      // a tile's route table is written (producer)
   uint64_t rempty[2];                     // ... and has been used (every epilogue warp)
   uint32_t tmem_base;
@@ -68,8 +79,11 @@ struct alignas(16) W4Ctl {
   uint8_t lead[kMaxBlocks];               // blocks in the group this block leads (0: not a group leader)
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * (kWBytes + kBBytes + kSBytes) + sizeof(W4Ctl);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <int kN>
+constexpr size_t smem_bytes_w4() {
+  return 1024 + static_cast<size_t>(W4Cfg<kN>::kStages) * (kWBytes + W4Cfg<kN>::kBBytes + kSBytes) + sizeof(W4Ctl<kN>);
+}
+static_assert(smem_bytes_w4<64>() <= 232448 && smem_bytes_w4<16>() <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   int ok = 0;
@@ -93,7 +107,8 @@ __device__ __forceinline__ void tma_gather4_rows(uint32_t dst, const CUtensorMap
 
 // Tile -> (leading plan block b, weight tile wt, expert e, blocks in the group
 // nb); false if the tile has no work.
-__device__ __forceinline__ bool w4_tile(const W4GemmParams& p, const W4Ctl* ctl, int64_t tile, int64_t nvalid,
+template <class Ctl>
+__device__ __forceinline__ bool w4_tile(const W4GemmParams& p, const Ctl* ctl, int64_t tile, int64_t nvalid,
                                         int& b, int& wt, int& e, int& nb) {
   b = static_cast<int>(tile / p.ntw);
   wt = static_cast<int>(tile % p.ntw);
@@ -108,15 +123,23 @@ __device__ __forceinline__ bool w4_tile(const W4GemmParams& p, const W4Ctl* ctl,
   return nb > 0 && e >= 0 && e < p.E;
 }
 
+template <int kN>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
                         const __grid_constant__ CUtensorMap tmB, const W4GemmParams p) {
+  using C = W4Cfg<kN>;
+  using W4CtlT = W4Ctl<kN>;
+  constexpr int kMaxN = C::kMaxN;
+  constexpr int kStages = C::kStages;
+  constexpr int kBBytes = C::kBBytes;
+  constexpr int kTBufs = C::kTBufs;
+  constexpr uint32_t kBufCols = 4u * kMaxN;  // TMEM columns per buffer
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sW = smem;
   uint8_t* sB = sW + kStages * kWBytes;
   uint8_t* sS = sB + kStages * kBBytes;
-  W4Ctl* ctl = reinterpret_cast<W4Ctl*>(sS + kStages * kSBytes);
+  W4CtlT* ctl = reinterpret_cast<W4CtlT*>(sS + kStages * kSBytes);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -126,9 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1 + kEpiWarps);  // MMA commit + every epilogue warp (reads the scales)
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTBufs; ++i) {
       mbar_init(smem_u32(&ctl->tfull[i]), 1);
       mbar_init(smem_u32(&ctl->tempty[i]), kEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctl->rfull[i]), 1);
       mbar_init(smem_u32(&ctl->rempty[i]), kEpiWarps);
     }
@@ -246,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < p.nkb; ++kb) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          const uint32_t tb = it & 1u;
-          const uint32_t tph = (it >> 1) & 1u;
+          const uint32_t tb = it % kTBufs;
+          const uint32_t tph = (it / kTBufs) & 1u;
           if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag) ||
               !mbar_wait(smem_u32(&ctl->tempty[tb]), tph ^ 1u, abort_flag)) {
             ok = false;
@@ -259,14 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // each 32-wide K block into its own columns: the epilogue scales them apart
 #pragma unroll
           for (int kk = 0; kk < kTK / 32; ++kk)
-            umma_f8(tmem_base + tb * 256u + kk * kMaxN, sw128_kmajor_desc(w0 + 32u * kk),
+            umma_f8(tmem_base + tb * kBufCols + kk * kMaxN, sw128_kmajor_desc(w0 + 32u * kk),
                     sw128_kmajor_desc(b0 + 32u * kk), idesc, 0u);
           umma_commit(smem_u32(&ctl->empty[s]));
           umma_commit(smem_u32(&ctl->tfull[tb]));
           ++it;
         }
       }
-      if (it > 0) drain_wait(smem_u32(&ctl->tfull[(it - 1) & 1u]), ((it - 1) >> 1) & 1u);
+      if (it > 0) drain_wait(smem_u32(&ctl->tfull[(it - 1) % kTBufs]), ((it - 1) / kTBufs) & 1u);
     }
     __syncwarp();
   } else if (warp == kLoaderWarp) {
@@ -333,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < p.nkb; ++kb) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
-        const uint32_t tb = it & 1u;
-        const uint32_t tph = (it >> 1) & 1u;
+        const uint32_t tb = it % kTBufs;
+        const uint32_t tph = (it / kTBufs) & 1u;
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ok) ok = warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag);
         if (ok) sc = *reinterpret_cast<const float4*>(sS + s * kSBytes + 16 * row);
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c8 = 0; c8 < kMaxN / 16; ++c8) {
               if (8 * c8 < ncols) {
                 uint32_t v[8];
-                tmem_ld_32x32b_x8(lane_base + tb * 256u + kk * kMaxN + c0 + 8 * c8, v);
+                tmem_ld_32x32b_x8(lane_base + tb * kBufCols + kk * kMaxN + c0 + 8 * c8, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[8 * c8 + i] = __fmaf_rn(__uint_as_float(v[i]), scl[kk], acc[8 * c8 + i]);
@@ -418,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool w4a8_tc_supported(int H, int I, int block_m, const void* w13, const void* w2, const void* w13_scale,
                        const void* w2_scale) {
   auto al = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
-  return H % 128 == 0 && I % 128 == 0 && block_m <= kMaxN && al(w13, 32) && al(w2, 32) && al(w13_scale, 16) &&
+  return H % 128 == 0 && I % 128 == 0 && block_m <= 64 && al(w13, 32) && al(w2, 32) && al(w13_scale, 16) &&
          al(w2_scale, 16);
 }
 
@@ -428,10 +453,17 @@ moe_status launch_w4a8_tc_gemm(const W4GemmTensors& t, W4GemmParams p, int sms, 
   MOE_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
   if (!attr_done[dev]) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(w4a8_tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmemBytes)));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(w4a8_tc_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem_bytes_w4<64>())));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(w4a8_tc_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem_bytes_w4<16>())));
     attr_done[dev] = true;
   }
+  // small plans (at most 16 tokens, so at most 16 routes per expert from
+  // distinct top-k ids, and plan blocks of at most 16 rows) take the narrow
+  // tiles with eight TMEM buffers
+  const bool narrow = p.block_m <= 16 && p.R <= 16 * p.top_k;
+  const int max_n = narrow ? 16 : 64;
   // weights: packed E2M1 rows of K codes (K/2 bytes), read as 16U4_ALIGN16B
   // boxes of 128 codes x (64 or 128) rows; scales: FP32 rows of K/32, boxes
   // of 4 x rows; gathered rows: E4M3, boxes of 128 codes x 1 row.
@@ -443,13 +475,16 @@ moe_status launch_w4a8_tc_gemm(const W4GemmTensors& t, W4GemmParams p, int sms, 
                                  (t.k / 32) * 4, 4, wrows, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
       encode_tensor_map_2d(&mb, t.rows, t.k, t.rows_total, t.k, kTK, 1, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
-  p.group = p.block_m >= kMaxN ? 1 : kMaxN / p.block_m;
+  p.group = p.block_m >= max_n ? 1 : max_n / p.block_m;
   p.rows_total = static_cast<int64_t>(t.rows_total);
   p.nkb = static_cast<int>(t.k / kTK);
   const int64_t tiles = p.nblocks * p.ntw;
   if (tiles <= 0) return MOE_OK;
   const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-  w4a8_tc_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mw, ms, mb, p);
+  if (narrow)
+    w4a8_tc_gemm_kernel<16><<<grid, kThreads, smem_bytes_w4<16>(), stream>>>(mw, ms, mb, p);
+  else
+    w4a8_tc_gemm_kernel<64><<<grid, kThreads, smem_bytes_w4<64>(), stream>>>(mw, ms, mb, p);
   MOE_CUDA_TRY(cudaGetLastError());
   return MOE_OK;
 }
