@@ -466,10 +466,15 @@ moe_status launch_w4a8_tc_gemm(const W4GemmTensors& t, W4GemmParams p, int sms, 
   // small plans (at most 16 tokens, so at most 16 routes per expert from
   // distinct top-k ids, and plan blocks of at most 16 rows) take the 16-row
   // tiles with eight TMEM buffers; other plans with blocks of at most 32 rows
-  // the 32-row tiles with four (measured at the page's shape: 64 tokens
-  // 0.91 -> 0.71 ms, 4096 tokens 6.17 -> 5.65 ms, 1024 tokens unchanged)
+  // the 32-row tiles with four -- except the gate/up projection when an
+  // expert holds 16-64 routes on average, where 32-row groups would stream
+  // many experts' weights twice (measured at the page's shape, forward:
+  // 64 tokens 0.91 -> 0.71 ms, 1024 tokens 1.58 -> 1.54 ms, 4096 tokens
+  // 6.17 -> 5.65 ms against 64-row tiles throughout)
   const bool narrow = p.block_m <= 16 && p.R <= 16 * p.top_k;
-  const bool mid = !narrow && p.block_m <= 32;
+  const int64_t touched = p.R < p.E ? p.R : p.E;
+  const int64_t per_expert = touched > 0 ? p.R / touched : 0;
+  const bool mid = !narrow && p.block_m <= 32 && !(p.up && per_expert > 16 && per_expert <= 64);
   const int max_n = narrow ? 16 : (mid ? 32 : 64);
   // weights: packed E2M1 rows of K codes (K/2 bytes), read as 16U4_ALIGN16B
   // boxes of 128 codes x (64 or 128) rows; scales: FP32 rows of K/32, boxes
