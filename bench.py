@@ -710,6 +710,8 @@ def extra_sweep(cfg, prob, flush, peaks):
     del base
     for label, (M, E, k) in (("router_m1", (1, 257, 9)), ("router_m8192", (8192, 288, 8))):
         out[label] = measure_router(M, E, k, flush, peaks)
+    for label, M in (("route_plan_m1", 1), ("route_plan_m8", 8)):
+        out[label] = measure_route_plan(M, 257, 9, 64, flush)
     torch.cuda.empty_cache()
     for M in (1, 1024):
         try:  # the E2M1-K32 path's timing must not hide the rest of the sweep
@@ -783,6 +785,47 @@ def measure_router(M, E, k, flush, peaks, steps=20, warmup=5):
     nbytes = M * E * 4 + M * k * 8
     return {"M": M, "E": E, "top_k": k, "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+
+def measure_route_plan(M, E, k, block_m, flush, steps=20, warmup=5):
+    """Router + plan for a decode step: moe_route_plan (one launch) against
+    moe_route_topk followed by moe_plan (two launches), each timed alone with
+    CUDA events, L2 flushed before each timed call."""
+    import torch
+    from fp8_block_scale_gb300 import _lib as L
+    g = torch.Generator(device="cpu").manual_seed(M * 131 + E)
+    logits = torch.randn((M, E), generator=g).cuda()
+    ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+    cap, bcap = L.moe_plan_capacity(M, k, E, block_m)
+    sids = torch.empty(cap, dtype=torch.int32, device="cuda")
+    eids = torch.empty(bcap, dtype=torch.int32, device="cuda")
+    ntpp = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(L.moe_plan_workspace_size(M, k, E), 256), dtype=torch.uint8, device="cuda")
+
+    def fused():
+        L.moe_route_plan(logits, k, ids, w, block_m, sids, eids, ntpp)
+
+    def two():
+        L.moe_route_topk(logits, k, ids, w)
+        L.moe_plan(ids, E, block_m, sids, eids, ntpp, ws)
+
+    res = {"M": M, "E": E, "top_k": k, "block_m": block_m}
+    for name, fn in (("ms_fused", fused), ("ms_router_then_plan", two)):
+        for _ in range(warmup):
+            fn()
+        times = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    return res
 
 
 def main():

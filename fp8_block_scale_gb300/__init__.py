@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     moe_quantize_act_per_row,
     moe_quantize_weight_128x128,
     moe_quantize_weight_k32,
+    moe_route_plan,
     moe_route_topk,
     moe_requant_scales_ue8m0,
     moe_status_string,

@@ -120,6 +120,10 @@ _SIGS = {
     "moe_route_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_void_p]),
+    "moe_route_plan": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_void_p]),
     "moe_quantize_act_1x128": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]),
     "moe_quantize_act_1x128_ue8m0": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
@@ -267,6 +271,19 @@ def moe_route_topk(logits, top_k, topk_ids, topk_weights, routed_scale=1.0, reno
     _check("moe_route_topk", load().moe_route_topk(
         _ptr(logits), dtype, M, E, top_k, float(routed_scale), 1 if renormalize else 0, _ptr(topk_ids), bits,
         _ptr(topk_weights), _stream(stream)))
+
+
+def moe_route_plan(logits, top_k, topk_ids, topk_weights, block_m, sorted_token_ids, expert_ids,
+                   num_tokens_post_padded, routed_scale=1.0, renormalize=True, stream=None):
+    """Router and plan in one launch (M * top_k <= 1024, E <= 1024): the
+    outputs of moe_route_topk, then of moe_plan on those ids."""
+    M, E = logits.shape
+    dtype = {torch.float32: LOGITS_F32, torch.bfloat16: LOGITS_BF16}[logits.dtype]
+    bits = {torch.int32: 32, torch.int64: 64}[topk_ids.dtype]
+    _check("moe_route_plan", load().moe_route_plan(
+        _ptr(logits), dtype, M, E, top_k, float(routed_scale), 1 if renormalize else 0, _ptr(topk_ids), bits,
+        _ptr(topk_weights), block_m, _ptr(sorted_token_ids), sorted_token_ids.numel(), _ptr(expert_ids),
+        expert_ids.numel(), _ptr(num_tokens_post_padded), _stream(stream)))
 
 
 def moe_quantize_act_1x128(x_bf16, q, scale, stream=None):

@@ -15,6 +15,7 @@
 //   3. scatter: sorted_token_ids[base(chunk, e) + rank] = r.
 // No inter-CTA waits; the same ids always give the same bytes.
 #include "common.cuh"
+#include "router.cuh"
 
 namespace moe {
 namespace {
@@ -218,25 +219,17 @@ __global__ void __launch_bounds__(kChunk) plan_scatter_kernel(const void* ids, i
   if (MOE_IN_BOUNDS(base + rk >= 0 && base + rk < ws.sorted_cap)) sorted_ids[base + rk] = static_cast<int32_t>(r);
 }
 
-// The whole plan in one CTA for R <= kSmallRoutes and E <= kSmallMaxExperts:
-// one route per thread, ranked by a warp match plus per-warp expert
-// histograms, then the padded expert scan and the scatter.  Same bytes as the
-// three-launch path (a stable counting sort).
-__global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* ids, int id_bits, int64_t R, int E,
-                                                                   int block_m, int32_t* sorted_ids,
-                                                                   int32_t* expert_ids, int32_t* num_post_padded,
-                                                                   int64_t sorted_cap, int64_t blocks_cap) {
-  extern __shared__ int32_t wh[];  // [32][E]: per-warp counts, then their exclusive prefix over warps
-  __shared__ int scan_smem[33];
-  __shared__ int totals[kSmallMaxExperts];
-  __shared__ int seg[kSmallMaxExperts];
+// The single-CTA plan: thread r < R holds its route's expert e (-1 for a
+// route the plan drops).  wh is [32][E] ints of dynamic shared memory.
+__device__ __forceinline__ void plan_small_body(int e, int64_t R, int E, int block_m, int32_t* sorted_ids,
+                                                int32_t* expert_ids, int32_t* num_post_padded, int64_t sorted_cap,
+                                                int64_t blocks_cap, int32_t* wh, int* scan_smem, int* totals,
+                                                int* seg) {
   constexpr int kWarps = kScanThreads / 32;
-  plan_enter();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r = threadIdx.x;
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wh[i] = 0;
   __syncthreads();
-  const int r = threadIdx.x;
-  const int e = r < R ? load_id(ids, id_bits, r, E) : -1;
   const unsigned peers = __match_any_sync(0xffffffffu, e);
   const unsigned below = peers & ((1u << lane) - 1u);
   const int in_warp = __popc(below);
@@ -279,6 +272,65 @@ __global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* id
     const int q = seg[e] + wh[warp * E + e] + in_warp;
     if (MOE_IN_BOUNDS(q >= 0 && q < sorted_cap)) sorted_ids[q] = static_cast<int32_t>(r);
   }
+}
+
+// The whole plan in one CTA for R <= kSmallRoutes and E <= kSmallMaxExperts:
+// one route per thread, ranked by a warp match plus per-warp expert
+// histograms, then the padded expert scan and the scatter.  Same bytes as the
+// three-launch path (a stable counting sort).
+__global__ void __launch_bounds__(kScanThreads) plan_small_kernel(const void* ids, int id_bits, int64_t R, int E,
+                                                                   int block_m, int32_t* sorted_ids,
+                                                                   int32_t* expert_ids, int32_t* num_post_padded,
+                                                                   int64_t sorted_cap, int64_t blocks_cap) {
+  extern __shared__ int32_t wh[];  // [32][E]: per-warp counts, then their exclusive prefix over warps
+  __shared__ int scan_smem[33];
+  __shared__ int totals[kSmallMaxExperts];
+  __shared__ int seg[kSmallMaxExperts];
+  plan_enter();
+  const int r = threadIdx.x;
+  const int e = r < R ? load_id(ids, id_bits, r, E) : -1;
+  plan_small_body(e, R, E, block_m, sorted_ids, expert_ids, num_post_padded, sorted_cap, blocks_cap, wh, scan_smem,
+                  totals, seg);
+}
+
+// Router and plan in one CTA (R <= kSmallRoutes, E <= kSmallMaxExperts): a
+// warp per token selects its top_k experts exactly as the router kernel does
+// and writes the ids and weights, keeping the ids in shared memory; then the
+// single-CTA plan runs on them.
+template <int kPer>
+__global__ void __launch_bounds__(kScanThreads) route_plan_kernel(const void* logits, int dtype, int64_t M, int E,
+                                                                   int top_k, float routed_scale, int renormalize,
+                                                                   void* ids, int id_bits, float* weights,
+                                                                   int block_m, int32_t* sorted_ids,
+                                                                   int32_t* expert_ids, int32_t* num_post_padded,
+                                                                   int64_t sorted_cap, int64_t blocks_cap) {
+  extern __shared__ int32_t wh[];  // [32][E]
+  __shared__ int s_e[kSmallRoutes];
+  __shared__ int scan_smem[33];
+  __shared__ int totals[kSmallMaxExperts];
+  __shared__ int seg[kSmallMaxExperts];
+  plan_enter();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t R = M * top_k;
+  for (int64_t t = warp; t < M; t += kScanThreads / 32) {
+    int id;
+    float w;
+    route_token<kPer>(logits, dtype, t, E, top_k, routed_scale, renormalize, id, w);
+    if (lane < top_k) {
+      const int64_t o = t * top_k + lane;
+      weights[o] = w;
+      if (id_bits == 64)
+        static_cast<int64_t*>(ids)[o] = id;
+      else
+        static_cast<int32_t*>(ids)[o] = id;
+      if (MOE_IN_BOUNDS(o < kSmallRoutes)) s_e[o] = (id >= 0 && id < E) ? id : -1;
+    }
+  }
+  __syncthreads();
+  const int r = threadIdx.x;
+  const int e = r < R ? s_e[r] : -1;
+  plan_small_body(e, R, E, block_m, sorted_ids, expert_ids, num_post_padded, sorted_cap, blocks_cap, wh, scan_smem,
+                  totals, seg);
 }
 
 size_t plan_ws_bytes(int64_t R, int E, int64_t* nchunks_out) {
@@ -360,6 +412,62 @@ moe_status moe_plan(const void* topk_ids, int id_bits, int64_t M, int top_k, int
                             topk_ids, id_bits, R, E, ws, sorted_token_ids));
   }
   return MOE_OK;
+}
+
+moe_status moe_route_plan(const void* logits, int logit_dtype, int64_t M, int E, int top_k, float routed_scale,
+                          int renormalize, void* topk_ids, int id_bits, float* topk_weights, int block_m,
+                          int32_t* sorted_token_ids, int64_t sorted_cap, int32_t* expert_ids, int64_t blocks_cap,
+                          int32_t* num_tokens_post_padded, moe_stream_t stream) {
+  using namespace moe;
+  if (logit_dtype != MOE_LOGITS_F32 && logit_dtype != MOE_LOGITS_BF16) return MOE_ERR_DTYPE;
+  if (id_bits != 32 && id_bits != 64) return MOE_ERR_DTYPE;
+  if (M < 0 || E < 1 || E > kSmallMaxExperts || top_k < 1 || top_k > kRouteMaxTopK || top_k > E) return MOE_ERR_SHAPE;
+  if (block_m < 8 || block_m > 1024 || block_m % 8 != 0) return MOE_ERR_SHAPE;
+  if (M * static_cast<int64_t>(top_k) > kSmallRoutes) return MOE_ERR_SHAPE;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_ERR_NULL;
+  if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_NULL;
+  int64_t need_cap = 0, need_blocks = 0;
+  moe_plan_capacity(M, top_k, E, block_m, &need_cap, &need_blocks);
+  if (sorted_cap < need_cap || blocks_cap < need_blocks) return MOE_ERR_CAPACITY;
+  DeviceInfo dev;
+  if (current_device(&dev) != MOE_OK) return MOE_ERR_CUDA;
+  if ((M > 0 && (!on_device(logits, dev.device) || !on_device(topk_ids, dev.device) ||
+                 !on_device(topk_weights, dev.device))) ||
+      !on_device(sorted_token_ids, dev.device) || !on_device(expert_ids, dev.device) ||
+      !on_device(num_tokens_post_padded, dev.device))
+    return MOE_ERR_DEVICE;
+  static bool attr_set[64] = {};
+  if (!attr_set[dev.device]) {
+    const int smem = (kScanThreads / 32) * kSmallMaxExperts * 4;
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(route_plan_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    attr_set[dev.device] = true;
+  }
+  const size_t smem = static_cast<size_t>(kScanThreads / 32) * E * sizeof(int32_t);
+  const int per = static_cast<int>(ceil_div(static_cast<int64_t>(E), int64_t(32)));
+  cudaError_t err;
+#define MOE_ROUTE_PLAN(K)                                                                                          \
+  launch_pdl(route_plan_kernel<K>, dim3(1), dim3(kScanThreads), smem, stream, 1, logits, logit_dtype, M, E, top_k, \
+             routed_scale, renormalize, topk_ids, id_bits, topk_weights, block_m, sorted_token_ids, expert_ids,   \
+             num_tokens_post_padded, sorted_cap, blocks_cap)
+  if (per <= 1)
+    err = MOE_ROUTE_PLAN(1);
+  else if (per <= 2)
+    err = MOE_ROUTE_PLAN(2);
+  else if (per <= 4)
+    err = MOE_ROUTE_PLAN(4);
+  else if (per <= 8)
+    err = MOE_ROUTE_PLAN(8);
+  else if (per <= 16)
+    err = MOE_ROUTE_PLAN(16);
+  else
+    err = MOE_ROUTE_PLAN(32);
+#undef MOE_ROUTE_PLAN
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -14,19 +14,12 @@
 // (value, index) and a warp argmax over (value descending, index ascending),
 // so the selection compares input values only and is exact.
 #include "common.cuh"
+#include "router.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouteMaxE = 2048;
-constexpr int kRouteMaxTopK = 32;
 constexpr int kRouteWarps = 8;
-
-__device__ __forceinline__ float load_logit(const void* logits, int dtype, int64_t i) {
-  if (dtype == 0) return static_cast<const float*>(logits)[i];
-  const uint32_t bits = static_cast<const uint16_t*>(logits)[i];
-  return __uint_as_float(bits << 16);  // BF16 -> FP32 is exact
-}
 
 template <int kPer>  // logits per lane: E <= 32 * kPer
 __global__ void __launch_bounds__(32 * kRouteWarps) route_topk_kernel(const void* logits, int dtype, int64_t M,
@@ -41,61 +34,16 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_topk_kernel(const void
   const int lane = threadIdx.x % 32;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + threadIdx.x / 32;
   if (t >= M) return;  // whole warp
-  float v[kPer];
-  uint64_t taken = 0;  // bit i: expert lane + 32 i already selected, or past E
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? load_logit(logits, dtype, t * E + e) : 0.f;
-    if (e >= E) taken |= uint64_t(1) << i;
-  }
-  constexpr int kNone = 0x7fffffff;
-  float my_l = 0.f;  // lane j < top_k: logit and expert of the j-th selection
-  int my_id = 0;
-  for (int j = 0; j < top_k; ++j) {
-    float bv = 0.f;
-    int bi = kNone;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && (bi == kNone || v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == (bi & 31)) taken |= uint64_t(1) << (bi >> 5);
-    if (lane == j) {
-      my_l = bv;
-      my_id = bi;
-    }
-  }
-  const float m = __shfl_sync(0xffffffffu, my_l, 0);  // the largest logit
-  const float num = lane < top_k ? expf(my_l - m) : 0.f;
-  float part = num;
-  if (!renormalize) {
-    part = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (lane + 32 * i < E) part += expf(v[i] - m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  int id;
+  float w;
+  route_token<kPer>(logits, dtype, t, E, top_k, routed_scale, renormalize, id, w);
   if (lane < top_k) {
     const int64_t o = t * top_k + lane;
-    weights[o] = num / part * routed_scale;
+    weights[o] = w;
     if (id_bits == 64)
-      static_cast<int64_t*>(ids)[o] = my_id;
+      static_cast<int64_t*>(ids)[o] = id;
     else
-      static_cast<int32_t*>(ids)[o] = my_id;
+      static_cast<int32_t*>(ids)[o] = id;
   }
 }
 

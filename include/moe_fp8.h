@@ -184,6 +184,22 @@ moe_status moe_quantize_weight_128x128(const uint16_t* w, int64_t E, int rows, i
 moe_status moe_route_topk(const void* logits, int logit_dtype, int64_t M, int E, int top_k, float routed_scale,
                           int renormalize, void* topk_ids, int id_bits, float* topk_weights, moe_stream_t stream);
 
+/* Router and plan in one launch, for small problems (decode): the ids and
+ * weights moe_route_topk writes, then the plan moe_plan builds from those
+ * ids, bit-identical to the two calls in sequence but without the second
+ * launch or a round trip through global memory between them (one CTA: a
+ * warp per token selects, then the single-CTA plan runs on the ids held in
+ * shared memory).  Arguments are those of the two calls; no plan workspace
+ * is needed.  Limits: M * top_k <= 1024 and E <= 1024, else MOE_ERR_SHAPE
+ * (use the two calls); otherwise the checks and errors of both calls
+ * (M == 0 writes an empty plan, P = 0).  Meant for a few tokens: the one
+ * CTA routes 32 tokens at a time, so from a few dozen tokens on the two
+ * calls, whose router spreads the tokens over many SMs, are faster. */
+moe_status moe_route_plan(const void* logits, int logit_dtype, int64_t M, int E, int top_k, float routed_scale,
+                          int renormalize, void* topk_ids, int id_bits, float* topk_weights, int block_m,
+                          int32_t* sorted_token_ids, int64_t sorted_cap, int32_t* expert_ids, int64_t blocks_cap,
+                          int32_t* num_tokens_post_padded, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * The fused forward (PR #4287 commit summary and "Public contract and review
  * fixes"; post-dot scale application, "Final W8 kernel performance (v46)").

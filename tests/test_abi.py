@@ -256,3 +256,28 @@ def test_debug_bounds_switch_without_gpu(lib, debug_lib):
     assert debug_lib.moe_debug_bounds_enabled() == 1
     missing = [name for name in _declared_functions() if not hasattr(debug_lib, name)]
     assert not missing, missing
+
+
+def test_route_plan_host_validation_without_gpu(lib):
+    """moe_route_plan rejects bad arguments on the host, before any device call."""
+    f = lib.moe_route_plan
+    p = _fake(4096)
+    ok = dict(logits=p, dtype=0, M=4, E=64, k=4, scale=1.0, renorm=1, ids=p, bits=32, w=p, bm=64,
+              s=p, cap=4096, e=p, bcap=64, ntpp=p)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["logits"], a["dtype"], a["M"], a["E"], a["k"], a["scale"], a["renorm"], a["ids"], a["bits"],
+                 a["w"], a["bm"], a["s"], a["cap"], a["e"], a["bcap"], a["ntpp"], None)
+    assert call(dtype=2) == 5                      # logit dtype
+    assert call(bits=16) == 5                      # id width
+    assert call(E=1025) == 2                       # more experts than the one-CTA plan takes
+    assert call(M=129, k=8) == 2                   # 1032 routes > 1024
+    assert call(k=65) == 2
+    assert call(k=0) == 2
+    assert call(bm=12) == 2
+    assert call(M=-1) == 2
+    assert call(s=None) == 1
+    assert call(logits=None) == 1
+    assert call(cap=10) == 4                       # plan capacity
+

@@ -86,3 +86,54 @@ def test_route_topk_feeds_the_plan():
     assert P == rP
     assert np.array_equal(sorted_ids[:P].cpu().numpy(), rs)
     assert np.array_equal(expert_ids[:P // bm].cpu().numpy(), rb)
+
+
+# ------------------------------------------------------------ router + plan in one launch
+
+ROUTE_PLAN_CASES = [
+    # (M, E, top_k, block_m, logit dtype, id dtype, renormalize)
+    (1, 257, 9, 64, torch.float32, torch.int32, True),      # decode_m1
+    (8, 257, 9, 64, torch.bfloat16, torch.int64, True),     # decode_m8, BF16 logits, int64 ids
+    (64, 257, 9, 64, torch.float32, torch.int32, False),    # decode_m64, plain softmax weights
+    (113, 288, 9, 16, torch.float32, torch.int32, True),    # 1017 routes, ragged blocks
+    (1024, 1024, 1, 128, torch.float32, torch.int32, True), # the largest R and E
+    (16, 8, 2, 8, torch.float32, torch.int32, True),        # E < 32
+    (0, 64, 4, 64, torch.float32, torch.int32, True),       # no tokens: an empty plan
+]
+
+
+@pytest.mark.parametrize("M,E,k,bm,dtype,id_dtype,renorm", ROUTE_PLAN_CASES,
+                         ids=[f"m{c[0]}-e{c[1]}-k{c[2]}-bm{c[3]}" for c in ROUTE_PLAN_CASES])
+def test_route_plan_matches_the_two_calls(M, E, k, bm, dtype, id_dtype, renorm):
+    """moe_route_plan writes the same ids, weights and plan, byte for byte,
+    as moe_route_topk followed by moe_plan on the same logits (every
+    capacity entry compared, including the pads and the blocks past P)."""
+    rng = np.random.default_rng(M * 31 + E + k)
+    logits = torch.from_numpy((rng.standard_normal((max(M, 1), E)) * 2.0).astype(np.float32)[:M]).to(dtype).cuda()
+    cap, bcap = L.moe_plan_capacity(M, k, E, bm)
+
+    def buffers():
+        return (torch.full((M, k), -7, dtype=id_dtype, device="cuda"),
+                torch.full((M, k), float("nan"), dtype=torch.float32, device="cuda"),
+                torch.full((cap,), -3, dtype=torch.int32, device="cuda"),
+                torch.full((bcap,), -3, dtype=torch.int32, device="cuda"),
+                torch.full((1,), -3, dtype=torch.int32, device="cuda"))
+
+    ids1, w1, s1, e1, p1 = buffers()
+    if M > 0:
+        L.moe_route_topk(logits, k, ids1, w1, 2.5, renorm)
+    ws = torch.empty(max(L.moe_plan_workspace_size(M, k, E), 256), dtype=torch.uint8, device="cuda")
+    L.moe_plan(ids1, E, bm, s1, e1, p1, ws)
+    ids2, w2, s2, e2, p2 = buffers()
+    L.moe_route_plan(logits, k, ids2, w2, bm, s2, e2, p2, 2.5, renorm)
+    torch.cuda.synchronize()
+    assert torch.equal(ids1, ids2)
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
+    assert int(p1.item()) == int(p2.item())
+    assert torch.equal(s1, s2)
+    assert torch.equal(e1, e2)
+    if M > 0:
+        exact = logits.float().cpu().numpy().astype(np.float64)
+        rid, rw = R.route_topk(exact, k, 2.5, renorm)
+        assert np.array_equal(ids2.cpu().numpy(), rid)
+        np.testing.assert_allclose(w2.cpu().numpy(), rw, rtol=WEIGHT_RTOL, atol=0)
