@@ -6,9 +6,9 @@
 // One persistent, warp-specialised kernel serves both projections.  Its
 // tiles are swapped against the FP8 path's: the MMA's M operand is 128
 // weight rows (tcgen05 kind::f8f6f4 takes E2M1 as one operand and E4M3 as
-// the other), its N operand the route rows of a plan block group (up to 64:
-// consecutive plan blocks of one expert are taken together, so an expert's
-// weights stream through once per group).  A weight row's K32 scale then
+// the other), its N operand the route rows of a plan block group (up to 64,
+// 32 or 16 by the kernel's width: consecutive plan blocks of one expert are
+// taken together, so an expert's weights stream through once per group).  A weight row's K32 scale then
 // belongs to one TMEM lane, and the epilogue promotes each 32-wide K block's
 // partial with a single per-thread scalar.
 //
@@ -17,9 +17,11 @@
 //               reads: 16U4_ALIGN16B, 128-byte swizzle), the weight rows' four
 //               K32 scales, and the group's activation (gate/up) or
 //               intermediate (down) rows gathered by token or route id
-//               (tile::gather4), into a 6-stage ring;
+//               (tile::gather4), into a 6- or 8-stage ring, one box per
+//               lane (a thread issues its copies one after another);
 //   warp 1      TMEM allocation and the MMA thread: four K = 32 MMAs per
-//               slice, each into its own N columns of one of two TMEM buffers;
+//               slice, each into its own N columns of one of the 2, 4 or 8
+//               TMEM buffers;
 //   warps 2..9  epilogue: warp w owns TMEM lane quarter w % 4 (32 weight
 //               rows) and half of the route columns; per slice it adds each
 //               K32 partial times its row's scale to FP32 registers;
