@@ -96,3 +96,24 @@ def test_noalloc_forward_under_bounds_checks():
     torch.cuda.synchronize()
     _no_failures("noalloc decode_m8")
     F._check(prob, np.arange(prob.cfg.M), label="debug-bounds noalloc")
+
+
+@pytest.mark.parametrize("M,E,k,bm", [(1, 257, 9, 64), (113, 288, 9, 16), (1024, 1024, 1, 128)])
+def test_route_plan_under_bounds_checks(M, E, k, bm):
+    """Router and plan in one launch: no check fails, and the plan matches
+    moe_plan on the ids it wrote."""
+    rng = np.random.default_rng(M + E)
+    logits = torch.from_numpy((rng.standard_normal((M, E)) * 2.0).astype(np.float32)).cuda()
+    cap, bcap = L.moe_plan_capacity(M, k, E, bm)
+    ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+    s1 = torch.full((cap,), -3, dtype=torch.int32, device="cuda")
+    e1 = torch.full((bcap,), -3, dtype=torch.int32, device="cuda")
+    p1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.moe_route_plan(logits, k, ids, w, bm, s1, e1, p1)
+    _no_failures(f"route_plan m{M}")
+    s2, e2, p2 = s1.clone().fill_(-3), e1.clone().fill_(-3), p1.clone()
+    ws = torch.empty(max(L.moe_plan_workspace_size(M, k, E), 256), dtype=torch.uint8, device="cuda")
+    L.moe_plan(ids, E, bm, s2, e2, p2, ws)
+    _no_failures(f"plan m{M}")
+    assert torch.equal(s1, s2) and torch.equal(e1, e2) and int(p1.item()) == int(p2.item())
